@@ -1,0 +1,302 @@
+// up_compact and up_scatter_back: the token-stream side of UniPrefill ("UniPrefill: Universal
+// Long-Context Prefill Acceleration via Block-wise Dynamic Sparsification", arXiv 2605.06221):
+// compaction of the kept tokens with the patched query_start_loc / seq_lens / num_actual_tokens
+// and the drop-history record (section 3.5, "vLLM scheduler integration"), and the end-of-block
+// carry-forward of Eq. 8 (section 3.4).
+//
+// Compaction is four launches, none of which waits on another CTA:
+//   count   per 4096-token tile, the number of kept tokens (16-byte loads of the byte mask)
+//   scan    one CTA: tile offsets, and per request prefix(cu[r]) = kept tokens before cu[r]
+//           -> new_cu_seqlens, new_seq_lens, num_actual_tokens, kept_len[layer], drop_layer[layer]
+//   index   per tile: block scan of the flags -> kept_index, out_positions, out_slots
+//   rows    row gather out_hidden[k] = hidden[kept_index[k]] with 16-byte vector copies, one warp
+//           per row, several loads in flight per lane (HBM bound: 2 * T' * hdim * 2 bytes)
+// Scatter-back is the row copy in the other direction: residual[kept_index[k]] = new_states[k].
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "up_internal.cuh"
+
+namespace up {
+namespace compact {
+
+constexpr int kTile = 4096;          // tokens per tile
+constexpr int kTileThreads = 256;    // 16 flags per thread
+constexpr int kRowThreads = 512;
+constexpr int kRowUnroll = 4;
+
+struct Layout {
+    size_t tile_cnt, tile_off, total;
+};
+
+static Layout layout(int64_t T) {
+    Layout L{};
+    const int64_t tiles = cdiv(T, kTile) + 1;
+    L.tile_cnt = 0;
+    L.tile_off = align_up(sizeof(int) * tiles, 256);
+    L.total = L.tile_off + align_up(sizeof(int) * tiles, 256);
+    return L;
+}
+
+__device__ __forceinline__ int count_nonzero_bytes(uint4 v) {
+    // number of non-zero bytes in 16 flag bytes
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    int c = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t x = w[i];
+        const uint32_t nz = ((x & 0x7F7F7F7Fu) + 0x7F7F7F7Fu | x) & 0x80808080u;   // high bit set where byte != 0
+        c += __popc(nz);
+    }
+    return c;
+}
+
+__device__ __forceinline__ uint4 load_flags16(const uint8_t* f, int64_t t0, int64_t T) {
+    if (t0 + 16 <= T) return *reinterpret_cast<const uint4*>(f + t0);
+    uint8_t b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) b[i] = (t0 + i < T) ? f[t0 + i] : 0;
+    uint4 v;
+    v.x = b[0] | (b[1] << 8) | (b[2] << 16) | ((uint32_t)b[3] << 24);
+    v.y = b[4] | (b[5] << 8) | (b[6] << 16) | ((uint32_t)b[7] << 24);
+    v.z = b[8] | (b[9] << 8) | (b[10] << 16) | ((uint32_t)b[11] << 24);
+    v.w = b[12] | (b[13] << 8) | (b[14] << 16) | ((uint32_t)b[15] << 24);
+    return v;
+}
+
+__device__ __forceinline__ int block_reduce_256(int v, int* sh) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) sh[w] = v;
+    __syncthreads();
+    int t = 0;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kTileThreads / 32; ++i) t += sh[i];
+        sh[8] = t;
+    }
+    __syncthreads();
+    t = sh[8];
+    __syncthreads();
+    return t;
+}
+
+__global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __restrict__ keep, int T, int* tile_cnt) {
+    __shared__ int sh[9];
+    const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
+    const int c = t0 < T ? count_nonzero_bytes(load_flags16(keep, t0, T)) : 0;
+    const int tot = block_reduce_256(c, sh);
+    if (threadIdx.x == 0) tile_cnt[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu,
+                                                    int R, int T, const int* tile_cnt, int* tile_off,
+                                                    int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
+                                                    int32_t* kept_len, uint8_t* drop_layer, int layer,
+                                                    int32_t* status) {
+    __shared__ int sh[32];
+    __shared__ int s_bad;
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (tid == 0) s_bad = 0;
+    __syncthreads();
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int c0 = cu[r], c1 = cu[r + 1];
+        if ((r == 0 && c0 != 0) || c1 < c0 || c1 > T || (r == R - 1 && c1 != T)) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (tid == 0) {
+            set_status(status, UP_DEV_BAD_CU_SEQLENS);
+            *num_actual = 0;
+        }
+        return;
+    }
+    // exclusive scan of the tile counts (tiles split in contiguous chunks over the threads)
+    const int tiles = (T + kTile - 1) / kTile;
+    const int per = (tiles + blockDim.x - 1) / blockDim.x;
+    const int a0 = min(tiles, tid * per), a1 = min(tiles, a0 + per);
+    int local = 0;
+    for (int i = a0; i < a1; ++i) local += tile_cnt[i];
+    int x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[w] = x;
+    __syncthreads();
+    if (w == 0) {
+        int s = sh[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        sh[lane] = s;
+    }
+    __syncthreads();
+    int off = (w > 0 ? sh[w - 1] : 0) + x - local;
+    for (int i = a0; i < a1; ++i) {
+        tile_off[i] = off;
+        off += tile_cnt[i];
+    }
+    __syncthreads();
+    // kept tokens before each request boundary: one warp per boundary
+    for (int r = w; r <= R; r += blockDim.x / 32) {
+        const int x0 = cu[r];
+        const int tile = x0 / kTile;
+        int c = 0;
+        for (int t = tile * kTile + lane; t < x0; t += 32) c += keep[t] != 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        const int before = (tile < tiles ? tile_off[tile] : (tiles > 0 ? tile_off[tiles - 1] + tile_cnt[tiles - 1] : 0)) + c;
+        if (lane == 0) new_cu[r] = before;
+    }
+    __syncthreads();
+    for (int r = tid; r < R; r += blockDim.x) {
+        const int len = new_cu[r + 1] - new_cu[r];
+        new_len[r] = len;
+        if (kept_len) kept_len[(int64_t)layer * R + r] = len;
+    }
+    if (tid == 0) {
+        *num_actual = new_cu[R];
+        if (drop_layer) drop_layer[layer] = 1;
+    }
+}
+
+__global__ void __launch_bounds__(kTileThreads) index_kernel(const uint8_t* __restrict__ keep, int T,
+                                                             const int* __restrict__ tile_off,
+                                                             const int64_t* __restrict__ pos,
+                                                             const int64_t* __restrict__ slots, int32_t* kept_index,
+                                                             int64_t* out_pos, int64_t* out_slots) {
+    __shared__ int sh[16];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
+    const uint4 f = t0 < T ? load_flags16(keep, t0, T) : make_uint4(0, 0, 0, 0);
+    const int c = count_nonzero_bytes(f);
+    int x = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sh[w] = x;
+    __syncthreads();
+    int base = tile_off[blockIdx.x];
+    for (int i = 0; i < w; ++i) base += sh[i];
+    int d = base + x - c;
+    const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        if ((fw[i >> 2] >> (8 * (i & 3))) & 0xFFu) {
+            const int64_t src = t0 + i;
+            kept_index[d] = static_cast<int32_t>(src);
+            if (out_pos) out_pos[d] = pos[src];
+            if (out_slots) out_slots[d] = slots[src];
+            ++d;
+        }
+    }
+}
+
+// dst[row_d(k)] = src[row_s(k)] for k < *count; one warp per row, 16-byte vectors
+template <bool GATHER>
+__global__ void __launch_bounds__(kRowThreads) rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                           const int32_t* __restrict__ idx,
+                                                           const int32_t* __restrict__ count, int64_t T_upper,
+                                                           int V, int32_t* status) {
+    const int n = *count;
+    if (n < 0 || n > T_upper) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, UP_DEV_BAD_TOKEN_COUNT);
+        return;
+    }
+    const int lane = threadIdx.x & 31;
+    const int warps = gridDim.x * (kRowThreads / 32);
+    for (int k = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); k < n; k += warps) {
+        const int64_t other = idx[k];
+        const uint4* s = src + (GATHER ? other : (int64_t)k) * V;
+        uint4* d = dst + (GATHER ? (int64_t)k : other) * V;
+        int j = lane;
+        for (; j + 32 * (kRowUnroll - 1) < V; j += 32 * kRowUnroll) {
+            uint4 r[kRowUnroll];
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) r[u] = __ldcs(s + j + 32 * u);
+#pragma unroll
+            for (int u = 0; u < kRowUnroll; ++u) d[j + 32 * u] = r[u];
+        }
+        for (; j < V; j += 32) d[j] = __ldcs(s + j);
+    }
+}
+
+}  // namespace compact
+}  // namespace up
+
+using namespace up;
+
+extern "C" size_t up_compact_workspace_bytes(int R, int64_t T) {
+    if (R <= 0 || T < 0 || T >= (int64_t(1) << 31)) return 0;
+    return compact::layout(T).total;
+}
+
+extern "C" up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seqlens, int R, int64_t T,
+                                const uint16_t* hidden, int hdim, const int64_t* positions, const int64_t* slots,
+                                uint16_t* out_hidden, int64_t* out_positions, int64_t* out_slots,
+                                int32_t* kept_index, int32_t* new_cu_seqlens, int32_t* new_seq_lens,
+                                int32_t* num_actual_tokens, int32_t* kept_len, uint8_t* drop_layer, int L, int layer,
+                                void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+    if (!token_keep || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens || !num_actual_tokens ||
+        !ws || !dev_status)
+        return UP_ERR_ARG;
+    if (R <= 0 || T < 0 || T >= (int64_t(1) << 31)) return UP_ERR_ARG;
+    if ((hidden == nullptr) != (out_hidden == nullptr) || (positions == nullptr) != (out_positions == nullptr) ||
+        (slots == nullptr) != (out_slots == nullptr))
+        return UP_ERR_ARG;
+    if ((kept_len || drop_layer) && (layer < 0 || layer >= L)) return UP_ERR_ARG;
+    if (hidden && (hdim <= 0 || hdim % 8 != 0 || !aligned16(hidden) || !aligned16(out_hidden))) return UP_ERR_SHAPE;
+    if (!aligned16(token_keep) || !aligned16(ws)) return UP_ERR_SHAPE;
+    const compact::Layout Lw = compact::layout(T);
+    if (ws_bytes < Lw.total) return UP_ERR_WORKSPACE;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int* tile_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + Lw.tile_cnt);
+    int* tile_off = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + Lw.tile_off);
+    const int tiles = static_cast<int>(cdiv(T, compact::kTile));
+    const int Ti = static_cast<int>(T);
+    if (tiles > 0) {
+        compact::count_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_cnt);
+        count_launch();
+    }
+    compact::scan_kernel<<<1, 1024, 0, st>>>(token_keep, cu_seqlens, R, Ti, tile_cnt, tile_off, new_cu_seqlens,
+                                             new_seq_lens, num_actual_tokens, kept_len, drop_layer, layer,
+                                             dev_status);
+    count_launch();
+    if (tiles > 0) {
+        compact::index_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_off, positions, slots,
+                                                                      kept_index, out_positions, out_slots);
+        count_launch();
+        if (hidden) {
+            const int V = hdim / 8;
+            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T, compact::kRowThreads / 32), 4 * num_sms()));
+            compact::rows_kernel<true><<<grid, compact::kRowThreads, 0, st>>>(
+                reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), kept_index,
+                num_actual_tokens, T, V, dev_status);
+            count_launch();
+        }
+    }
+    return check_launch();
+}
+
+extern "C" up_status up_scatter_back(const uint16_t* new_states, const int32_t* kept_index,
+                                     const int32_t* num_actual_tokens, int64_t T_upper, int hdim, uint16_t* residual,
+                                     int32_t* dev_status, void* stream) {
+    if (!new_states || !kept_index || !num_actual_tokens || !residual || !dev_status) return UP_ERR_ARG;
+    if (T_upper < 0 || T_upper >= (int64_t(1) << 31)) return UP_ERR_ARG;
+    if (hdim <= 0 || hdim % 8 != 0 || !aligned16(new_states) || !aligned16(residual)) return UP_ERR_SHAPE;
+    if (T_upper == 0) return UP_OK;
+    const int V = hdim / 8;
+    const int grid = static_cast<int>(std::min<int64_t>(cdiv(T_upper, compact::kRowThreads / 32), 4 * num_sms()));
+    compact::rows_kernel<false><<<grid, compact::kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        reinterpret_cast<const uint4*>(new_states), reinterpret_cast<uint4*>(residual), kept_index, num_actual_tokens,
+        T_upper, V, dev_status);
+    count_launch();
+    return check_launch();
+}
