@@ -1,0 +1,381 @@
+"""Throughput of UniPrefill's per-layer drop step on GB300, through the C ABI.
+
+One step = one pass of the whole hot path over one batch:
+  up_score_blocks (Eqs. 2-4) -> up_select_topp (Eq. 5/14) -> up_compact (+ metadata, history)
+  -> up_slot_mapping (Eq. 16, next layer) -> up_scatter_back (Eq. 8) -> up_seqused (Eq. 17)
+value = tokens of the batch / device time of one step (CUDA events on the launching stream).
+
+Default workload: LLaMA-3.1-8B full-attention layer, one request of 32768 tokens (32/8 heads,
+d_k 128, hidden 4096, G 64, n 128, A 128, p 0.99), synthetic seeded bf16 inputs.  L2 is
+flushed (512 MB write) before every timed step.  `--impl reference` times the fp64 CPU oracle
+on the host cores instead (bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill tokens/s through score+top-p+compact; % of tensor/HBM roofline"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload index 1..5 (default 2: LLaMA-3.1-8B, 32K)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clocks and throttle reasons while the GPU is under load."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index=0, period_ms=20):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", f"-lms={period_ms}"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((ts, float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 <= r[0] <= t1] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i, v in enumerate(r[3]) if v.lower().startswith("active")})
+        return {"sm_mhz": statistics.median([r[1] for r in inside]) if inside else None,
+                "sm_max_mhz": max([r[2] for r in inside]) if inside else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------------------------ our arm
+
+def run_gb300(args, w, rank, world):
+    import torch
+    import long_context_prefill_varlen_gb300 as up
+    from synth import cpu as gen
+    from synth import gpu as sgpu
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    up.load_library()
+    stream = torch.cuda.current_stream()
+
+    inputs = sgpu.build_device(w, device=dev)
+    cu = inputs["cu_seqlens"]
+    L, layer, B = 4, 1, 16
+    step = up.DropStep(cu, w.T, w.Hq, w.Hkv, w.dk, w.hdim, G=w.G, n=w.n, A=w.A, p=w.p, L=L, layer=layer,
+                       device=dev)
+    mb = max(1, max(-(-N // B) for N in w.lengths))
+    rng = np.random.default_rng(12345)
+    table = torch.from_numpy(rng.permutation(w.R * mb).reshape(w.R, mb).astype(np.int32)).to(dev)
+    next_slots = torch.empty(max(1, w.T), dtype=torch.int64, device=dev)
+    residual = inputs["hidden"].clone()
+    orig_len = torch.tensor(w.lengths, dtype=torch.int32, device=dev)
+    kv_len = orig_len.clone()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def run_step(marks=None):
+        def mark(i):
+            if marks is not None:
+                marks[i].record(stream)
+        mark(0)
+        step.score(inputs["Q"], inputs["K"])
+        mark(1)
+        step.select()
+        mark(2)
+        step.compact(inputs["hidden"], inputs["positions"], inputs["slots"])
+        mark(3)
+        up.up_slot_mapping(step.out_positions[:w.T], step.new_cu, table, B, next_slots, step.status,
+                           num_tokens=step.num_actual)
+        mark(4)
+        step.scatter_back(step.out_hidden, residual)
+        mark(5)
+        step.seqused(orig_len, kv_len, layer + 1)
+        mark(6)
+
+    for _ in range(max(3, args.warmup)):
+        flush.fill_(1)
+        run_step()
+    torch.cuda.synchronize()
+    step.check()
+    kept = int(step.num_actual.item())
+
+    nst = 7
+    marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(args.steps)]
+    sampler = ClockSampler(dev.index) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches0 = up.up_kernel_launches()
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.fill_(1)                      # L2 flush, outside the event pair
+        run_step(marks[k])
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    launches = up.up_kernel_launches() - launches0
+    if world > 1:
+        torch.distributed.barrier()
+    clocks = sampler.stop(t0, t1) if sampler else None
+    step.check()
+
+    stage_ms = np.zeros((args.steps, nst - 1))
+    for k in range(args.steps):
+        for i in range(nst - 1):
+            stage_ms[k, i] = marks[k][i].elapsed_time(marks[k][i + 1])
+    step_ms = stage_ms.sum(axis=1)
+    ms = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    return dict(ms=ms, stage_ms=stage_ms.mean(axis=0), launches=launches, clocks=clocks, kept=kept,
+                kstar=step.kstar.cpu().tolist(), step=step, inputs=inputs, run_step=run_step, dev=dev,
+                flush=flush)
+
+
+def e2e_measure(args, w, ctx):
+    """Same step through the C ABI with the batch in pinned HOST memory: H2D of the inputs the calls read,
+    the step, D2H of its result (the compacted stream and its metadata), all inside the timed region."""
+    import torch
+    step, inp, dev = ctx["step"], ctx["inputs"], ctx["dev"]
+    pin = {k: inp[k].cpu().pin_memory() for k in ("K", "hidden", "positions", "slots")}
+    Qh = inp["Q"].cpu().pin_memory()
+    cu = w.cu_seqlens()
+    wins = [(max(cu[r], cu[r + 1] - w.n), cu[r + 1]) for r in range(w.R)]     # the query rows the score reads
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    h2d += sum((b - a) * w.Hq * w.dk * 2 for a, b in wins)
+    out_h = torch.empty(w.T, w.hdim, dtype=torch.bfloat16).pin_memory()
+    out_p = torch.empty(w.T, dtype=torch.int64).pin_memory()
+    out_s = torch.empty(w.T, dtype=torch.int64).pin_memory()
+    meta = torch.empty(w.R + 1, dtype=torch.int32).pin_memory()
+    times, d2h = [], 0
+    for it in range(args.e2e_steps + 1):
+        ctx["flush"].fill_(1)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for k in pin:
+            inp[k].copy_(pin[k], non_blocking=True)
+        for a, b in wins:
+            inp["Q"][a:b].copy_(Qh[a:b], non_blocking=True)
+        ctx["run_step"]()
+        n_act = int(step.num_actual.item())               # the host learns T' here
+        out_h[:n_act].copy_(step.out_hidden[:n_act], non_blocking=True)
+        out_p[:n_act].copy_(step.out_positions[:n_act], non_blocking=True)
+        out_s[:n_act].copy_(step.out_slots[:n_act], non_blocking=True)
+        meta.copy_(step.new_cu, non_blocking=True)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if it > 0:
+            times.append(t1 - t0)
+        d2h = 4 + n_act * (w.hdim * 2 + 16) + (w.R + 1) * 4
+    sec = statistics.mean(times)
+    return {"value": w.T / sec, "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "ms_per_step": sec * 1e3, "steps": len(times)}
+
+
+# ------------------------------------------------------------------------------------------ oracle timing
+
+def oracle_sample(w, sample_tokens):
+    """Inputs of a bounded sample: one request of `sample_tokens` tokens with the workload's geometry
+    (the workload itself when it is a single request of that length)."""
+    from synth import cpu as gen
+    if w.R == 1 and w.T == sample_tokens:
+        ws = w
+    else:
+        ws = w.replace(lengths=(int(sample_tokens),), salt=w.index * 7 + 1)
+    host = gen.materialize(ws)
+    Q = gen.bf16_bits_to_f32(host["Q"]).astype(np.float64)
+    K = gen.bf16_bits_to_f32(host["K"]).astype(np.float64)
+    return ws, host, Q, K
+
+
+def oracle_once(ws, host, Q, K):
+    import oracle
+    t0 = time.perf_counter()
+    out = oracle.drop_step(Q, K, host["cu_seqlens"], ws.G, ws.n, ws.A, ws.p, host["hidden"],
+                           host["positions"], host["slots"])
+    c = out["compact"]
+    oracle.carry_forward(host["hidden"], c["hidden"], c["kept_index"])
+    return time.perf_counter() - t0
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    sample = min(w.T, 4096)
+    sw = oracle_sample(w, sample)
+    for _ in range(args.warmup):
+        oracle_once(*sw)
+    times = [oracle_once(*sw) for _ in range(args.steps)]
+    sec = statistics.mean(times)
+    val = sample / sec
+    cores = cpu_cores()
+    return {"metric": METRIC, "value": val, "unit": UNIT, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w),
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"one request of {sample} tokens with the workload's geometry per step "
+                                       "(score+select+compact+scatter; the per-token work does not depend on N)"},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------------------------------ report
+
+def workload_config(w):
+    return {"workload": w.name, "R": w.R, "T": w.T, "Hq": w.Hq, "Hkv": w.Hkv, "d_k": w.dk, "hidden": w.hdim,
+            "G": w.G, "n": w.n, "A": w.A, "p": w.p, "seed": w.seed, "l2": "flushed (512 MB write) before each step",
+            "parallelism": "request-sharded replicas, no collective on the data path"}
+
+
+def score_flops(w):
+    """Algorithmic FLOPs of both passes: 2 * d_k * (n_eff*N - n_eff(n_eff-1)/2) per (request, query head, pass)."""
+    tot = 0
+    for N in w.lengths:
+        ne = min(w.n, N)
+        tot += 2 * w.dk * (ne * N - ne * (ne - 1) // 2) * w.Hq * 2
+    return tot
+
+
+def main():
+    args = parse()
+    rank, world = int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        if args.impl == "reference":
+            dist.init_process_group("gloo")
+        else:
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+            dist.init_process_group("nccl")
+    from synth import recipe
+    w = recipe.workload(args.config)
+    if args.impl == "reference":
+        line = run_reference(args, w, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    res = run_gb300(args, w, rank, world)
+    if rank != 0:
+        return
+    pk, pk_kind = peaks()
+    ms = res["ms"]
+    T_all = w.T * world
+    st = res["stage_ms"]
+    names = ["score", "select", "compact", "slot_mapping", "scatter_back", "seqused"]
+    kept = res["kept"]
+    hb = w.hdim * 2
+    flops = score_flops(w)
+    bytes_rows = 2 * kept * hb                                  # read + write of every kept row
+    stages = {}
+    for i, nm in enumerate(names):
+        stages[nm] = {"ms": float(st[i])}
+    stages["score"].update({"tflops": flops / (st[0] * 1e-3) / 1e12,
+                            "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"]})
+    for nm in ("compact", "scatter_back"):
+        i = names.index(nm)
+        gbs = (bytes_rows + kept * 4) / (st[i] * 1e-3) / 1e9
+        stages[nm].update({"gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]})
+    stages["select"]["us"] = float(st[1] * 1e3)
+    ssc = float(st[0] + st[1] + st[2])
+    # dominant single-kernel launch: scatter_back is one row-copy kernel (the same kernel as compact's gather)
+    sc_ms = float(st[4])
+    score_ms = float(st[0])
+    if score_ms >= sc_ms:
+        rl = {"bound": "tensor", "kernel": "score passes (tcgen05), plan+finalize included",
+              "achieved": flops / (score_ms * 1e-3) / 1e12, "peak": pk["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        rl = {"bound": "hbm", "kernel": "rows_kernel (up_scatter_back: 1 launch)",
+              "achieved": (bytes_rows + kept * 4) / (sc_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s"}
+    rl["frac"] = rl["achieved"] / rl["peak"]
+    rl["traffic"] = None
+    rl["peak_source"] = pk_kind
+    line = {"metric": METRIC, "value": T_all / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
+            "roofline": rl, "gpu_launches": int(res["launches"]), "clocks": res["clocks"],
+            "score_select_compact_tokens_per_s": T_all / (ssc * 1e-3), "kept_tokens": kept,
+            "kstar": res["kstar"][:8], "stages": stages}
+    if not args.no_e2e:
+        line["e2e"] = e2e_measure(args, w, res)
+    if world == 1 and not args.no_cpu_baseline:
+        sample = min(w.T, 32768)
+        sw = oracle_sample(w, sample)
+        sec = oracle_once(*sw)
+        line["cpu_baseline"] = {"value": sample / sec, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                                "seconds": sec,
+                                "sample": (f"the whole workload ({sample} tokens)" if sw[0] is w else
+                                           f"one request of {sample} tokens with the workload's geometry")
+                                          + ": score+select+compact+scatter in fp64 numpy, inputs excluded"}
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -122,7 +122,7 @@ up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const int32_t* c
  *   k* = min k with sum_{first k} b >= p * sum_g b  (sums in fp64);
  *   token_keep_i = [block(i) among the first k*] or i < A (sinks) or i >= N - n (window);
  *   block_keep_g = any token of B_g kept.
- * block_scores: fp32 [nb_cap], finite and >= 0.  p in (0, 1]; A >= 0; n >= 1.
+ * block_scores: fp32 [nb_cap], finite and >= 0.  p in (0, 1]; A >= 0; n >= 1; G a power of two.
  * block_keep: u8 [nb_cap]; token_keep: u8 [T]; kstar: int32 [R] (0 for empty requests).
  * At most UP_MAX_BLOCKS_PER_REQUEST blocks per request (else UP_DEV_TOO_MANY_BLOCKS). */
 up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,

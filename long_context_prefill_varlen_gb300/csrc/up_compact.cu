@@ -5,7 +5,7 @@
 // carry-forward of Eq. 8 (section 3.4).
 //
 // Compaction is four launches, none of which waits on another CTA:
-//   count   per 4096-token tile, the number of kept tokens (16-byte loads of the byte mask)
+//   count   per 1024-token tile, the number of kept tokens (16-byte loads of the byte mask)
 //   scan    one CTA: tile offsets, and per request prefix(cu[r]) = kept tokens before cu[r]
 //           -> new_cu_seqlens, new_seq_lens, num_actual_tokens, kept_len[layer], drop_layer[layer]
 //   index   per tile: block scan of the flags -> kept_index, out_positions, out_slots
@@ -21,8 +21,8 @@
 namespace up {
 namespace compact {
 
-constexpr int kTile = 4096;          // tokens per tile
-constexpr int kTileThreads = 256;    // 16 flags per thread
+constexpr int kTile = 1024;          // tokens per tile
+constexpr int kTileThreads = 64;     // 16 flags per thread
 constexpr int kRowThreads = 512;
 constexpr int kRowUnroll = 4;
 
@@ -65,7 +65,7 @@ __device__ __forceinline__ uint4 load_flags16(const uint8_t* f, int64_t t0, int6
     return v;
 }
 
-__device__ __forceinline__ int block_reduce_256(int v, int* sh) {
+__device__ __forceinline__ int block_reduce(int v, int* sh) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __re
     __shared__ int sh[9];
     const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
     const int c = t0 < T ? count_nonzero_bytes(load_flags16(keep, t0, T)) : 0;
-    const int tot = block_reduce_256(c, sh);
+    const int tot = block_reduce(c, sh);
     if (threadIdx.x == 0) tile_cnt[blockIdx.x] = tot;
 }
 

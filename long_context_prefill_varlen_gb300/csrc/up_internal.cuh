@@ -182,6 +182,18 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, uint32_t (&v)[64]) {
 // ------------------------------------------------------------------------------------------------
 // misc
 
+// true on exactly one lane of a converged warp (elect.sync); the issuing roles run their loops on
+// the whole warp so that operands stay warp-uniform, and issue asynchronous work from this lane
+__device__ __forceinline__ bool elect_one() {
+    uint32_t pred;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "elect.sync _|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(pred));
+    return pred != 0;
+}
+
 __device__ __forceinline__ float ex2(float x) {   // 2^x on the SFU (ex2.approx.ftz.f32)
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

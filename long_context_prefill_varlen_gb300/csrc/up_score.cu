@@ -5,20 +5,25 @@
 // For every request r, KV head kh and the group x n window query rows that read kh:
 //   pass 1  S = Qwin . K^T on tcgen05 (query rows in TMEM lanes, 128 keys per tile in columns);
 //           per row the online max m and sum l of 2^(S*a - m) over the causal key range;
-//           per work item (kItemTiles key tiles) a partial (m, l); the last CTA of each
-//           (r, kh, slab) unit merges the partials in a fixed order into c = m + log2(l).
+//           per work item (kItemTiles key tiles) a partial (m, l).
+//   merge   per query row, the partials of its (r, kh, slab) unit folded in a fixed order into
+//           c = m + log2(l) (one warp per row).
 //   pass 2  S^T = K . Qwin^T (128 keys in TMEM lanes, query rows in columns); each thread owns a
 //           key and sums P = 2^(S*a - c_row) over its rows; the per-key sums are reduced over G
 //           consecutive keys with warp shuffles and written as per-(unit, block) partials.
 //   final   b_g = (sum over units of the partials) / (n_eff * Hq * G).
 // a = sm_scale * log2(e): the softmax is computed in base 2, exactly equal to exp in base e.
 //
-// CTA layout (320 threads, one CTA per SM, persistent over a contiguous range of work items):
-//   warp 0   TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warp 1   TMEM allocator and single-thread tcgen05.mma issuer
-//   warps 2-9  two epilogue warpgroups; warpgroup w reads TMEM columns [64w, 64w+64) of every
-//              128x128 accumulator, so both share each job (a job = one 128x128 MMA tile)
+// CTA layout (576 threads, one CTA per SM, persistent over a contiguous range of work items):
+//   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 2-17 four epilogue warpgroups.  A job is one 128x128 fp32 accumulator; with J jobs per
+//              key tile, warpgroup g takes jobs g, g+4, ... when J >= 3, half a job (64 columns) when
+//              J = 2 and a quarter (32 columns) when J = 1.  TMEM is read in 16-column chunks, the
+//              next chunk's load in flight while the current one is reduced.
 // TMEM: 4 accumulators of 128 columns (the whole 512-column TMEM), used as a ring of jobs.
+// Per element the epilogue spends one ex2 on the SFU (32/clk/SM on this part, the same rate at
+// which the tensor core produces S elements at d_k = 128) plus packed f32x2 FMA/add work.
 #include <math.h>
 
 #include <algorithm>
@@ -34,13 +39,14 @@ constexpr int kStageBytes = 128 * 128;          // 128 rows x 64 bf16 (one 128-b
 constexpr int kStages = 5;
 constexpr int kSlabBytes = 128 * 1024;          // resident query rows of one unit
 constexpr int kItemTiles = 2;                   // key tiles per work item (pass-1 partial granularity)
-constexpr int kThreads = 320;
+constexpr int kEpiThreads = 512;
+constexpr int kThreads = 64 + kEpiThreads;
 constexpr int kMaxJ = 8;                        // 128-row jobs per slab (d_k = 64 -> 8)
 constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
 constexpr int kCtrlBytes = 256;
 constexpr int kCvecFloats = 1024;
-constexpr int kXchgBytes = kMaxJ * 128 * 8;
+constexpr int kXchgBytes = 4 * 2 * 128 * 8;     // pass 1: (m,l) of 4 warpgroups x 2 jobs
 constexpr int kSmemBytes = 1024 + kSlabBytes + kStages * kStageBytes + kCtrlBytes + kCvecFloats * 4 + kXchgBytes;
 
 struct Geometry {
@@ -48,7 +54,7 @@ struct Geometry {
 };
 
 struct Layout {
-    size_t items, unit_items, n_items, unit_done, ml, cvec, blk, tok, total;
+    size_t items, unit_items, n_items, ml, cvec, blk, tok, total;
     int64_t items_cap, units;
 };
 
@@ -61,7 +67,6 @@ struct Params {
     int4* items;
     int2* unit_items;
     int* n_items;
-    int* unit_done;
     float2* ml;
     float* cvec;
     float* blk;
@@ -97,11 +102,10 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
     L.items = take(sizeof(int4) * L.items_cap);
     L.unit_items = take(sizeof(int2) * L.units);
     L.n_items = take(16);
-    L.unit_done = take(sizeof(int) * L.units);
     L.ml = take(sizeof(float2) * L.items_cap * g.slab_rows);
     L.cvec = take(sizeof(float) * L.units * g.slab_rows);
-    L.blk = take(sizeof(float) * (size_t)Hkv * g.slabs * nb_cap);
-    L.tok = tok ? take(sizeof(float) * (size_t)Hkv * g.slabs * T) : 0;
+    L.blk = take(sizeof(float) * (size_t)Hkv * g.slabs * 4 * nb_cap);      // one partial per warpgroup
+    L.tok = tok ? take(sizeof(float) * (size_t)Hkv * g.slabs * 4 * T) : 0;
     L.total = o;
     return L;
 }
@@ -169,17 +173,30 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     int total = 0;
     int off = block_exclusive_scan_1024(local, s_scan, &total);
     for (int r = r0; r < r1; ++r) {
-        const int N = P.cu[r + 1] - P.cu[r];
-        const int ntiles = (N + kTileKeys - 1) / kTileKeys;
         const int ni = nitems(r);
         for (int kk = 0; kk < P.units_per_req; ++kk) {
             const int u = r * P.units_per_req + kk;
             P.unit_items[u] = make_int2(off + kk * ni, ni);
-            P.unit_done[u] = 0;
-            for (int s = 0; s < ni; ++s)
-                P.items[off + kk * ni + s] = make_int4(r, kk, s * kItemTiles, min(ntiles, (s + 1) * kItemTiles));
         }
         off += ni * P.units_per_req;
+    }
+    __syncthreads();
+    // every thread writes items: item `it` belongs to the largest request r whose first item is <= it
+    for (int it = tid; it < total; it += blockDim.x) {
+        int lo = 0, hi = P.R;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (P.unit_items[mid * P.units_per_req].x <= it) lo = mid; else hi = mid;
+        }
+        // the largest r with first_item(r) <= it is never an empty request (an empty request shares its
+        // first item with the next one, and it < total excludes an empty last request)
+        const int r = lo;
+        const int ni = nitems(r);
+        const int rel = it - P.unit_items[r * P.units_per_req].x;
+        const int kk = rel / ni, sidx = rel % ni;
+        const int N = P.cu[r + 1] - P.cu[r];
+        const int ntiles = (N + kTileKeys - 1) / kTileKeys;
+        P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
     }
     if (tid == 0) {
         P.n_items[0] = total;
@@ -202,7 +219,6 @@ struct Smem {
     uint64_t* mma_done;
     uint32_t* tmem_holder;
     int* abort_flag;
-    int* last_flag;
     float* cvec;           // [kCvecFloats]
     uint8_t* xchg;         // [kXchgBytes]
 };
@@ -223,7 +239,6 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.mma_done = b + 2 * kStages + 10;
     s.tmem_holder = reinterpret_cast<uint32_t*>(b + 2 * kStages + 11);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
-    s.last_flag = s.abort_flag + 1;
     s.cvec = reinterpret_cast<float*>(ctrl + kCtrlBytes);
     s.xchg = reinterpret_cast<uint8_t*>(s.cvec + kCvecFloats);
     return s;
@@ -233,16 +248,21 @@ struct ItemInfo {
     int r, kk, tb, te, unit, base, N, kh, slab;
 };
 
+// Values read from memory are not known to be warp-uniform; the MMA, TMA and TMEM-load operands
+// derived from them must be.  Broadcasting from lane 0 makes the uniformity explicit, so everything
+// computed from the schedule below stays in warp-uniform registers (every caller is a full warp).
+__device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
+
 __device__ __forceinline__ ItemInfo item_info(const Params& P, int it) {
     const int4 w = P.items[it];
     ItemInfo I;
-    I.r = w.x;
-    I.kk = w.y;
-    I.tb = w.z;
-    I.te = w.w;
+    I.r = uni(w.x);
+    I.kk = uni(w.y);
+    I.tb = uni(w.z);
+    I.te = uni(w.w);
     I.unit = I.r * P.units_per_req + I.kk;
-    I.base = P.cu[I.r];
-    I.N = P.cu[I.r + 1] - I.base;
+    I.base = uni(P.cu[I.r]);
+    I.N = uni(P.cu[I.r + 1]) - I.base;
     I.kh = I.kk / P.slabs;
     I.slab = I.kk % P.slabs;
     return I;
@@ -264,30 +284,35 @@ __device__ void drain_loads(const Smem& S, uint32_t stage_cnt, uint32_t slab_cnt
 template <int NC>
 __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ, const CUtensorMap* tmK,
                          int it0, int it1) {
+    // the whole warp walks the schedule (warp-uniform values); one elected lane issues the copies
     volatile int* abort_flag = S.abort_flag;
     int prev_unit = -1;
     uint32_t stage_cnt = 0, slab_cnt = 0;
     const uint32_t slab_addr = smem_u32(S.slab), stage_addr = smem_u32(S.stages);
+    const bool leader = elect_one();
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
         if (I.unit != prev_unit) {
-            if (!mbar_wait(smem_u32(S.slab_free), (slab_cnt & 1) ^ 1, abort_flag)) {
-                drain_loads(S, stage_cnt, slab_cnt);
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(S.slab_free), (slab_cnt & 1) ^ 1, abort_flag))) {
+                if (leader) drain_loads(S, stage_cnt, slab_cnt);
                 return;
             }
             const int row0 = I.slab * P.slab_rows;
             const int rows = min(P.slab_rows, P.rows_total - row0);
             const uint32_t bar = smem_u32(S.slab_full);
-            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * NC * 128u);
-            for (int qr = 0; qr < rows; qr += P.box_rows) {
-                const int qg = row0 + qr;
-                const int hl = qg / P.n, t0 = qg % P.n;
-                const int head = I.kh * P.group + hl;
-                const int tok = I.base + I.N - P.n + t0;      // may be < 0: TMA fills zeros
+            if (leader) {
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(rows) * NC * 128u);
+                for (int qr = 0; qr < rows; qr += P.box_rows) {
+                    const int qg = row0 + qr;
+                    const int hl = qg / P.n, t0 = qg % P.n;
+                    const int head = I.kh * P.group + hl;
+                    const int tok = I.base + I.N - P.n + t0;      // may be < 0: TMA fills zeros
 #pragma unroll
-                for (int c = 0; c < NC; ++c)
-                    tma_load_3d(slab_addr + c * P.slab_rows * 128 + qr * 128, tmQ, bar, c * 64, head, tok);
+                    for (int c = 0; c < NC; ++c)
+                        tma_load_3d(slab_addr + c * P.slab_rows * 128 + qr * 128, tmQ, bar, c * 64, head, tok);
+                }
             }
+            __syncwarp();
             ++slab_cnt;
             prev_unit = I.unit;
         }
@@ -295,35 +320,52 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
 #pragma unroll
             for (int c = 0; c < NC; ++c) {
                 const uint32_t s = stage_cnt % kStages, ph = (stage_cnt / kStages) & 1;
-                if (!mbar_wait(smem_u32(S.empty + s), ph ^ 1, abort_flag)) {
-                    drain_loads(S, stage_cnt, slab_cnt);
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(S.empty + s), ph ^ 1, abort_flag))) {
+                    if (leader) drain_loads(S, stage_cnt, slab_cnt);
                     return;
                 }
-                mbar_arrive_expect_tx(smem_u32(S.full + s), kStageBytes);
-                tma_load_3d(stage_addr + s * kStageBytes, tmK, smem_u32(S.full + s), c * 64, I.kh,
-                            I.base + kt * kTileKeys);
+                if (leader) {
+                    mbar_arrive_expect_tx(smem_u32(S.full + s), kStageBytes);
+                    tma_load_3d(stage_addr + s * kStageBytes, tmK, smem_u32(S.full + s), c * 64, I.kh,
+                                I.base + kt * kTileKeys);
+                }
+                __syncwarp();
                 ++stage_cnt;
             }
         }
     }
 }
 
+// Descriptor of a K-major SW128 operand advanced by `bytes` (a multiple of 16): the start address
+// occupies the low 14 bits as address >> 4 and every operand lies below 256 KB of shared memory, so
+// the advance is a plain add on the descriptor.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 template <int PASS, int NC>
 __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
     volatile int* abort_flag = S.abort_flag;
     int prev_unit = -1;
     uint32_t stage_cnt = 0, slab_cnt = 0, jc = 0;
-    const uint32_t slab_addr = smem_u32(S.slab), stage_addr = smem_u32(S.stages);
     const int J = P.J;
-    auto slab_desc = [&](int j, int c, int k) {   // 128 query rows of job j, k-chunk c, 16-wide slice k
-        return sdesc_sw128(slab_addr + c * P.slab_rows * 128 + j * 128 * 128 + k * 32);
+    // base descriptors: query slab at (chunk 0, row 0) and K stage 0; strides in bytes
+    const uint64_t slab_d0 = sdesc_sw128(smem_u32(S.slab));
+    const uint64_t stage_d0 = sdesc_sw128(smem_u32(S.stages));
+    const uint32_t slab_chunk_bytes = static_cast<uint32_t>(P.slab_rows) * 128u;   // one 64-wide k chunk
+    // the whole warp runs this loop with warp-uniform values; one elected lane issues the MMAs and
+    // the commits (a commit tracks the MMAs issued by its own thread)
+    const bool leader = elect_one();
+    auto wait_all = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, mbar_wait(bar, parity, abort_flag));
     };
-    auto stage_desc = [&](uint32_t s, int k) { return sdesc_sw128(stage_addr + s * kStageBytes + k * 32); };
+    auto commit = [&](uint32_t bar) {
+        if (leader) tc_commit(bar);
+        __syncwarp();
+    };
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
         if (I.unit != prev_unit) {
-            if (prev_unit >= 0) tc_commit(smem_u32(S.slab_free));
-            if (!mbar_wait(smem_u32(S.slab_full), slab_cnt & 1, abort_flag)) goto out;
+            if (prev_unit >= 0) commit(smem_u32(S.slab_free));
+            if (!wait_all(smem_u32(S.slab_full), slab_cnt & 1)) goto out;
             ++slab_cnt;
             tc_fence_after();
             prev_unit = I.unit;
@@ -333,227 +375,337 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                 // jobs outer: the tile's K stages stay resident while the J jobs run
                 for (int j = 0; j < J; ++j) {
                     const uint32_t buf = jc & 3;
-                    if (!mbar_wait(smem_u32(S.tempty + buf), ((jc >> 2) & 1) ^ 1, abort_flag)) goto out;
+                    if (!wait_all(smem_u32(S.tempty + buf), ((jc >> 2) & 1) ^ 1)) goto out;
                     tc_fence_after();
+                    const uint64_t qd = desc_add(slab_d0, j * 128 * 128);
+                    const uint32_t d_tmem = tmem_base + buf * 128;
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
                         const uint32_t sc = stage_cnt + c, s = sc % kStages;
                         if (j == 0) {
-                            if (!mbar_wait(smem_u32(S.full + s), (sc / kStages) & 1, abort_flag)) goto out;
+                            if (!wait_all(smem_u32(S.full + s), (sc / kStages) & 1)) goto out;
                             tc_fence_after();
                         }
+                        const uint64_t kd = desc_add(stage_d0, s * kStageBytes);
+                        const uint64_t qdc = desc_add(qd, c * slab_chunk_bytes);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = PASS == 1 ? slab_desc(j, c, k) : stage_desc(s, k);
-                            const uint64_t b = PASS == 1 ? stage_desc(s, k) : slab_desc(j, c, k);
-                            tc_mma_bf16(tmem_base + buf * 128, a, b, kIdesc, (c | k) != 0);
+                            const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
+                            const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
+                            if (leader) tc_mma_bf16(d_tmem, a, b, kIdesc, (c | k) != 0);
                         }
                     }
-                    tc_commit(smem_u32(S.tfull + buf));
+                    commit(smem_u32(S.tfull + buf));
                     ++jc;
                 }
 #pragma unroll
-                for (int c = 0; c < NC; ++c) tc_commit(smem_u32(S.empty + (stage_cnt + c) % kStages));
+                for (int c = 0; c < NC; ++c) commit(smem_u32(S.empty + (stage_cnt + c) % kStages));
                 stage_cnt += NC;
             } else {
                 // chunks outer (d_k = 256, J <= 2): each K stage is released as soon as all jobs used it
                 for (int j = 0; j < J; ++j) {
                     const uint32_t q = jc + j;
-                    if (!mbar_wait(smem_u32(S.tempty + (q & 3)), ((q >> 2) & 1) ^ 1, abort_flag)) goto out;
+                    if (!wait_all(smem_u32(S.tempty + (q & 3)), ((q >> 2) & 1) ^ 1)) goto out;
                 }
                 tc_fence_after();
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const uint32_t s = stage_cnt % kStages;
-                    if (!mbar_wait(smem_u32(S.full + s), (stage_cnt / kStages) & 1, abort_flag)) goto out;
+                    if (!wait_all(smem_u32(S.full + s), (stage_cnt / kStages) & 1)) goto out;
                     tc_fence_after();
+                    const uint64_t kd = desc_add(stage_d0, s * kStageBytes);
                     for (int j = 0; j < J; ++j) {
-                        const uint32_t buf = (jc + j) & 3;
+                        const uint32_t d_tmem = tmem_base + ((jc + j) & 3) * 128;
+                        const uint64_t qdc = desc_add(slab_d0, j * 128 * 128 + c * slab_chunk_bytes);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = PASS == 1 ? slab_desc(j, c, k) : stage_desc(s, k);
-                            const uint64_t b = PASS == 1 ? stage_desc(s, k) : slab_desc(j, c, k);
-                            tc_mma_bf16(tmem_base + buf * 128, a, b, kIdesc, (c | k) != 0);
+                            const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
+                            const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
+                            if (leader) tc_mma_bf16(d_tmem, a, b, kIdesc, (c | k) != 0);
                         }
                     }
-                    tc_commit(smem_u32(S.empty + s));
+                    commit(smem_u32(S.empty + s));
                     ++stage_cnt;
                 }
-                for (int j = 0; j < J; ++j) tc_commit(smem_u32(S.tfull + ((jc + j) & 3)));
+                for (int j = 0; j < J; ++j) commit(smem_u32(S.tfull + ((jc + j) & 3)));
                 jc += J;
             }
         }
     }
 out:
     // make sure no MMA is still running when the CTA tears down its TMEM
-    tc_commit(smem_u32(S.mma_done));
+    __syncwarp();
+    commit(smem_u32(S.mma_done));
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(smem_u32(S.mma_done), 0)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
 }
 
+// Job map of the epilogue (one place for both the dispatch and the epilogue): with J jobs per key
+// tile, wg_per_job(J) warpgroups share a job (each reads chunks_per_slice(J) 16-column chunks of it)
+// and warpgroup g takes the jobs g / wpj + u * (4 / wpj).  (Splitting J = 4 jobs over pairs of
+// warpgroups, so that each pair alternates between two TMEM buffers, measured slower: the per-job
+// overheads doubled.)
+__host__ __device__ constexpr int wg_per_job(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
+__host__ __device__ constexpr int chunks_per_slice(int J) { return 8 / wg_per_job(J); }
+static_assert(chunks_per_slice(1) == 2 && chunks_per_slice(2) == 4 && chunks_per_slice(3) == 8 &&
+                  chunks_per_slice(4) == 8 && chunks_per_slice(8) == 8,
+              "a job slice must cover 128 / wg_per_job columns");
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes, without waiting
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr)
+        : "memory");
+}
+// wait for every outstanding tcgen05.ld of this thread, then pin the destination registers after
+// the wait so that no use of them can be scheduled before it
+__device__ __forceinline__ void tmem_wait_pin(uint32_t (&v)[16]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]));
+}
+
+__device__ __forceinline__ float f(uint32_t x) { return __uint_as_float(x); }
+
+// pass 1, one 16-column chunk of one query row, every column visible: online (m, l) in base 2,
+// m = max S*a, l = sum 2^(S*a - m); the running sum is rescaled only when the max grows
+__device__ __forceinline__ void row_chunk_full(const uint32_t (&v)[16], float a, float& m, float& l) {
+    const float x0 = max3(f(v[0]), f(v[1]), f(v[2])), x1 = max3(f(v[3]), f(v[4]), f(v[5]));
+    const float x2 = max3(f(v[6]), f(v[7]), f(v[8])), x3 = max3(f(v[9]), f(v[10]), f(v[11]));
+    const float x4 = max3(f(v[12]), f(v[13]), f(v[14]));
+    const float mx = max3(max3(x0, x1, x2), max3(x3, x4, f(v[15])), x0) * a;
+    if (mx > m) {
+        l *= ex2(m - mx);
+        m = mx;
+    }
+    const float nm = -m;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+        s0 += ex2(fmaf(f(v[c]), a, nm));
+        s1 += ex2(fmaf(f(v[c + 1]), a, nm));
+        s2 += ex2(fmaf(f(v[c + 2]), a, nm));
+        s3 += ex2(fmaf(f(v[c + 3]), a, nm));
+    }
+    l += (s0 + s1) + (s2 + s3);
+}
+
+// pass 1 with the causal limit: columns c <= lim are visible
+__device__ __forceinline__ void row_chunk_masked(const uint32_t (&v)[16], int lim, float a, float& m, float& l) {
+    if (lim < 0) return;
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        if (c <= lim) mx = fmaxf(mx, f(v[c]));
+    mx *= a;
+    if (mx > m) {
+        l *= ex2(m - mx);
+        m = mx;
+    }
+    float sm = 0.f;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        if (c <= lim) sm += ex2(fmaf(f(v[c]), a, -m));
+    l += sm;
+}
+
+// pass 2, one 16-column chunk of one key, every row visible: sum of 2^(S*a - c_row); ncv holds -c_row
+// (-inf for rows that are not window rows of this request, which therefore contribute 0)
+__device__ __forceinline__ void key_chunk_full(const uint32_t (&v)[16], const float* ncv, float a, float (&acc)[4]) {
+    const float4* nc4 = reinterpret_cast<const float4*>(ncv);
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+        const float4 n = nc4[c / 4];
+        acc[0] += ex2(fmaf(f(v[c]), a, n.x));
+        acc[1] += ex2(fmaf(f(v[c + 1]), a, n.y));
+        acc[2] += ex2(fmaf(f(v[c + 2]), a, n.z));
+        acc[3] += ex2(fmaf(f(v[c + 3]), a, n.w));
+    }
+}
+
+// pass 2 with the causal mask: key i is visible to the query row at local position pos iff i <= pos
+__device__ __forceinline__ void key_chunk_masked(const uint32_t (&v)[16], const float* ncv, float a, int i, int qg0,
+                                                 int n, int N, int rows_total, float (&acc)[4]) {
+    if (i >= N) return;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+        const int qg = qg0 + c;
+        const int pos = N - n + (qg % n);
+        const bool vis = qg < rows_total && pos >= 0 && i <= pos;
+        const float p = ex2(fmaf(f(v[c]), a, ncv[c]));
+        acc[c & 3] += vis ? p : 0.f;
+    }
+}
+
+__device__ __forceinline__ void release_tmem(const Smem& S, uint32_t buf, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(S.tempty + buf));
+}
+
+struct JobCtx {
+    float a;
+    int lim0;          // pass 1: last visible column of the job slice (relative to its first column)
+    bool rvalid;       // pass 1: this thread's row is a window row of the request
+    bool fast;         // every element of the job slice is visible to this thread
+    int key, qg0, n, N, rows_total;
+    const float* ncv0;
+};
+
+// One job slice whose every element is visible to every thread of the warp: NCH 16-column chunks,
+// TMEM loads double-buffered (the next chunk in flight while the current one is reduced); the TMEM
+// buffer is released as soon as its last chunk has landed.  Straight-line code, kept compact.
+template <int PASS, int NCH>
+__device__ __forceinline__ void run_job_fast(const Smem& S, uint32_t ta, uint32_t buf, int lane, const JobCtx& c,
+                                             float& m, float& l, float (&acc)[4]) {
+    uint32_t va[16], vb[16];
+    tmem_ld16(ta, va);
+    tmem_wait_pin(va);
+#pragma unroll
+    for (int ch = 0; ch < NCH; ch += 2) {
+        tmem_ld16(ta + (ch + 1) * 16, vb);
+        if (PASS == 1) row_chunk_full(va, c.a, m, l);
+        else key_chunk_full(va, c.ncv0 + ch * 16, c.a, acc);
+        tmem_wait_pin(vb);
+        if (ch + 2 < NCH) tmem_ld16(ta + (ch + 2) * 16, va);
+        else release_tmem(S, buf, lane);
+        if (PASS == 1) row_chunk_full(vb, c.a, m, l);
+        else key_chunk_full(vb, c.ncv0 + (ch + 1) * 16, c.a, acc);
+        if (ch + 2 < NCH) tmem_wait_pin(va);
+    }
+}
+
+// The general case (tiles that reach into the causal window or past the request's end, and the
+// abort path): one chunk at a time with the masks; rare, so kept out of the fast path's code.
 template <int PASS>
+__device__ __noinline__ void run_job_slow(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool ok, int nch,
+                                          const JobCtx& c, float& m, float& l, float (&acc)[4]) {
+    for (int ch = 0; ch < nch; ++ch) {
+        uint32_t v[16];
+        if (ok) {
+            tmem_ld16(ta + ch * 16, v);
+            tmem_wait_pin(v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = 0u;
+        }
+        if (ch == nch - 1) release_tmem(S, buf, lane);
+        if (PASS == 1) {
+            if (c.rvalid) row_chunk_masked(v, c.lim0 - ch * 16, c.a, m, l);
+        } else {
+            key_chunk_masked(v, c.ncv0 + ch * 16, c.a, c.key, c.qg0 + ch * 16, c.n, c.N, c.rows_total, acc);
+        }
+    }
+}
+
+template <int PASS, int NCH>
 __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
     volatile int* abort_flag = S.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int et = threadIdx.x - 64;            // 0..255
-    const int wg = (warp - 2) >> 2;             // column half
+    const int et = threadIdx.x - 64;            // 0..511
+    const int wg = (warp - 2) >> 2;             // warpgroup 0..3
     const int q = warp & 3;                     // TMEM lane quarter this warp may access
     const int rl = q * 32 + lane;               // row (pass 1) or key (pass 2) inside a 128-tile
-    const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * 64;
     const float a = P.a;
     const int J = P.J;
-    uint32_t jc = 0;
+    const int wpj = wg_per_job(J);              // warpgroups per job
+    const int cols = NCH * 16;                  // columns this warpgroup reads per job = 128 / wpj
+    const int col0 = (wpj == 1 ? 0 : (wg % wpj) * cols);
+    const int jfirst = wg / wpj;
+    const int jstep = 4 / wpj;
+    const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + col0;
+    uint32_t tiles_done = 0;
     int prev_unit = -1;
     uint32_t tile_par = 0;
-    float m[kMaxJ], l[kMaxJ];
+    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;   // pass 1 state of the (<= 2) jobs
 
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
         const int ne = min(P.n, I.N);
         const int row0 = I.slab * P.slab_rows;   // first global query row of this slab
         if (PASS == 2 && I.unit != prev_unit) {
-            named_bar_sync(1, 256);
-            for (int i = et; i < P.slab_rows; i += 256) S.cvec[i] = __ldcg(P.cvec + (size_t)I.unit * P.slab_rows + i);
-            named_bar_sync(1, 256);
+            named_bar_sync(1, kEpiThreads);
+            for (int i = et; i < P.slab_rows; i += kEpiThreads)
+                S.cvec[i] = -__ldcg(P.cvec + (size_t)I.unit * P.slab_rows + i);
+            named_bar_sync(1, kEpiThreads);
         }
         prev_unit = I.unit;
         if (PASS == 1) {
-#pragma unroll
-            for (int j = 0; j < kMaxJ; ++j) {
-                m[j] = -INFINITY;
-                l[j] = 0.f;
-            }
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
         }
-        for (int kt = I.tb; kt < I.te; ++kt) {
-            float acc = 0.f;
-#pragma unroll
-            for (int j = 0; j < kMaxJ; ++j) {
-                if (j >= J) break;
+        for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
+            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            const bool tile_full = kt * kTileKeys + kTileKeys - 1 <= I.N - ne;
+            int u = 0;
+            for (int j = jfirst; j < J; j += jstep, ++u) {
+                const uint32_t jc = tiles_done * J + j;
                 const uint32_t buf = jc & 3;
-                // after an abort every wait fails fast; the warp then skips the TMEM read (warp-uniformly,
-                // tcgen05.ld is .sync.aligned) but keeps walking the same loop so the named barriers match
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (jc >> 2) & 1, abort_flag));
+                const bool ok =
+                    __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (jc >> 2) & 1, abort_flag));
                 tc_fence_after();
-                uint32_t v[64];
-                if (ok) {
-                    tmem_ld64(tl + buf * 128, v);
-                } else {
-#pragma unroll
-                    for (int c = 0; c < 64; ++c) v[c] = 0u;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(S.tempty + buf));
-                ++jc;
+                JobCtx c;
+                c.a = a;
+                const int qg_row = row0 + j * 128 + rl;                       // pass 1: this thread's row
+                const int pos_row = I.N - P.n + (qg_row % P.n);
+                c.rvalid = qg_row < P.rows_total && pos_row >= 0;
+                c.lim0 = pos_row - (kt * kTileKeys + col0);
+                c.key = kt * kTileKeys + rl;                                  // pass 2: this thread's key
+                c.qg0 = row0 + j * 128 + col0;
+                c.n = P.n;
+                c.N = I.N;
+                c.rows_total = P.rows_total;
+                c.ncv0 = S.cvec + j * 128 + col0;
+                c.fast = PASS == 1 ? (c.rvalid && c.lim0 >= cols - 1) : tile_full;
+                float mm = u ? m1 : m0, ll = u ? l1 : l0;
+                if (ok && __all_sync(0xffffffffu, c.fast))
+                    run_job_fast<PASS, NCH>(S, tl + buf * 128, buf, lane, c, mm, ll, acc);
+                else
+                    run_job_slow<PASS>(S, tl + buf * 128, buf, lane, ok, NCH, c, mm, ll, acc);
                 if (PASS == 1) {
-                    // thread = query row (row0 + 128 j + rl); columns = keys kt*128 + 64 wg + c
-                    const int qg = row0 + j * 128 + rl;
-                    const int pos = I.N - P.n + (qg % P.n);      // local position of this query
-                    if (qg < P.rows_total && pos >= 0) {
-                        const int key0 = kt * kTileKeys + wg * 64;
-                        const int lim = pos - key0;              // columns c <= lim are visible
-                        float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
-                        if (lim >= 63) {
-#pragma unroll
-                            for (int c = 0; c < 64; c += 4) {
-                                mx0 = fmaxf(mx0, __uint_as_float(v[c]));
-                                mx1 = fmaxf(mx1, __uint_as_float(v[c + 1]));
-                                mx2 = fmaxf(mx2, __uint_as_float(v[c + 2]));
-                                mx3 = fmaxf(mx3, __uint_as_float(v[c + 3]));
-                            }
-                        } else {
-#pragma unroll
-                            for (int c = 0; c < 64; ++c)
-                                if (c <= lim) mx0 = fmaxf(mx0, __uint_as_float(v[c]));
-                        }
-                        const float mx = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
-                        if (mx > -INFINITY) {
-                            const float mn = fmaxf(m[j], mx * a);
-                            float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                            if (lim >= 63) {
-#pragma unroll
-                                for (int c = 0; c < 64; c += 4) {
-                                    s0 += ex2(fmaf(__uint_as_float(v[c]), a, -mn));
-                                    s1 += ex2(fmaf(__uint_as_float(v[c + 1]), a, -mn));
-                                    s2 += ex2(fmaf(__uint_as_float(v[c + 2]), a, -mn));
-                                    s3 += ex2(fmaf(__uint_as_float(v[c + 3]), a, -mn));
-                                }
-                            } else {
-#pragma unroll
-                                for (int c = 0; c < 64; ++c)
-                                    if (c <= lim) s0 += ex2(fmaf(__uint_as_float(v[c]), a, -mn));
-                            }
-                            l[j] = l[j] * ex2(m[j] - mn) + ((s0 + s1) + (s2 + s3));
-                            m[j] = mn;
-                        }
-                    }
-                } else {
-                    // thread = key i (kt*128 + rl); columns = query rows 128 j + 64 wg + c of the slab
-                    const int i = kt * kTileKeys + rl;
-                    const float4* cv = reinterpret_cast<const float4*>(S.cvec + j * 128 + wg * 64);
-                    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
-                    if (kt * kTileKeys + kTileKeys - 1 <= I.N - ne) {
-                        // every key of the tile is visible to every window row; rows that are not
-                        // window rows carry c = +inf and contribute 2^-inf = 0
-#pragma unroll
-                        for (int c4 = 0; c4 < 16; ++c4) {
-                            const float4 cc = cv[c4];
-                            s0 += ex2(fmaf(__uint_as_float(v[4 * c4 + 0]), a, -cc.x));
-                            s1 += ex2(fmaf(__uint_as_float(v[4 * c4 + 1]), a, -cc.y));
-                            s2 += ex2(fmaf(__uint_as_float(v[4 * c4 + 2]), a, -cc.z));
-                            s3 += ex2(fmaf(__uint_as_float(v[4 * c4 + 3]), a, -cc.w));
-                        }
-                    } else if (i < I.N) {
-                        const int qbase = row0 + j * 128 + wg * 64;
-#pragma unroll
-                        for (int c4 = 0; c4 < 16; ++c4) {
-                            const float4 cc = cv[c4];
-                            const float cw[4] = {cc.x, cc.y, cc.z, cc.w};
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int qg = qbase + 4 * c4 + e;
-                                const int pos = I.N - P.n + (qg % P.n);
-                                const bool vis = qg < P.rows_total && pos >= 0 && i <= pos;
-                                const float p = ex2(fmaf(__uint_as_float(v[4 * c4 + e]), a, -cw[e]));
-                                s0 += vis ? p : 0.f;
-                            }
-                        }
-                    }
-                    acc += (s0 + s1) + (s2 + s3);
+                    if (u) { m1 = mm; l1 = ll; } else { m0 = mm; l0 = ll; }
                 }
             }
             if (PASS == 2) {
-                // combine the two column halves, then reduce over G consecutive keys (fixed order)
-                float* xb = reinterpret_cast<float*>(S.xchg) + (tile_par & 1) * 128;
-                float* wsum = reinterpret_cast<float*>(S.xchg) + 256 + (tile_par & 1) * 4;
-                if (wg == 1) xb[rl] = acc;
-                named_bar_sync(1, 256);
-                if (wg == 0) {
-                    const float tot = acc + xb[rl];
-                    const int i = kt * kTileKeys + rl;
-                    if (P.tok != nullptr && i < I.N) P.tok[(size_t)I.kk * P.T + I.base + i] = tot;
-                    const int nb = (I.N + P.G - 1) / P.G;
-                    const int cb = P.cb[I.r];
-                    float* dst = P.blk + (size_t)I.kk * P.nb_cap + cb;
-                    float s = tot;
-                    const int gw = P.G < 32 ? P.G : 32;
-                    for (int o = gw >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                    if (P.G <= 32) {
-                        const int g = i / P.G;
-                        if ((lane & (P.G - 1)) == 0 && g < nb) dst[g] = s;
-                    } else {
-                        if (lane == 0) wsum[q] = s;
-                        named_bar_sync(2, 128);
-                        if (lane == 0) {
-                            if (P.G == 64 && (q & 1) == 0) {
-                                const int g = i / 64;
-                                if (g < nb) dst[g] = wsum[q] + wsum[q + 1];
-                            } else if (P.G == 128 && q == 0) {
-                                const int g = i / 128;
-                                if (g < nb) dst[g] = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
-                            }
+                // this warpgroup's per-key partial, reduced over G consecutive keys (keys are TMEM lanes,
+                // so warp shuffles, then the warps of the group for G > 32); one partial per warpgroup
+                const float tot = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                const int i = kt * kTileKeys + rl;
+                const size_t part = (size_t)I.kk * 4 + wg;
+                if (P.tok != nullptr && i < I.N) P.tok[part * P.T + I.base + i] = tot;
+                const int nb = (I.N + P.G - 1) / P.G;
+                float* dst = P.blk + part * P.nb_cap + P.cb[I.r];
+                float s = tot;
+                const int gw = P.G < 32 ? P.G : 32;
+                for (int o = gw >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (P.G <= 32) {
+                    const int g = i / P.G;
+                    if ((lane & (P.G - 1)) == 0 && g < nb) dst[g] = s;
+                } else {
+                    float* wsum = reinterpret_cast<float*>(S.xchg) + (tile_par & 1) * 16 + wg * 4;
+                    if (lane == 0) wsum[q] = s;
+                    named_bar_sync(2 + wg, 128);
+                    if (lane == 0) {
+                        if (P.G == 64 && (q & 1) == 0) {
+                            const int g = i / 64;
+                            if (g < nb) dst[g] = wsum[q] + wsum[q + 1];
+                        } else if (P.G == 128 && q == 0) {
+                            const int g = i / 128;
+                            if (g < nb) dst[g] = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
                         }
                     }
                 }
@@ -561,52 +713,64 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
             }
         }
         if (PASS == 1) {
-            // merge the two column halves per row, write this item's partial (m, l)
-            float2* xm = reinterpret_cast<float2*>(S.xchg);
-            if (wg == 1) {
-#pragma unroll
-                for (int j = 0; j < kMaxJ; ++j)
-                    if (j < J) xm[j * 128 + rl] = make_float2(m[j], l[j]);
-            }
-            named_bar_sync(1, 256);
-            if (wg == 0) {
-#pragma unroll
-                for (int j = 0; j < kMaxJ; ++j) {
-                    if (j < J) {
-                        const float2 o = xm[j * 128 + rl];
-                        const float mm = fmaxf(m[j], o.x);
-                        const float ll = mm == -INFINITY ? 0.f : l[j] * ex2(m[j] - mm) + o.y * ex2(o.x - mm);
-                        P.ml[(size_t)it * P.slab_rows + j * 128 + rl] = make_float2(mm, ll);
+            // merge the warpgroups that share a job (fixed order), write this item's partial (m, l)
+            // into the unit's block, laid out [row][item of the unit] for the merge kernel
+            const int2 ui = P.unit_items[I.unit];
+            float2* part = P.ml + (size_t)ui.x * P.slab_rows + (it - ui.x);
+            float2* xm = reinterpret_cast<float2*>(S.xchg);             // [4 warpgroups][2 jobs][128 rows]
+            if (wpj > 1) {
+                int u = 0;
+                for (int j = jfirst; j < J; j += jstep, ++u)
+                    xm[(wg * 2 + u) * 128 + rl] = u ? make_float2(m1, l1) : make_float2(m0, l0);
+                named_bar_sync(1, kEpiThreads);
+                if (wg % wpj == 0) {
+                    u = 0;
+                    for (int j = jfirst; j < J; j += jstep, ++u) {
+                        float mm = -INFINITY;
+                        for (int w2 = wg; w2 < wg + wpj; ++w2) mm = fmaxf(mm, xm[(w2 * 2 + u) * 128 + rl].x);
+                        float ll = 0.f;
+                        if (mm > -INFINITY)
+                            for (int w2 = wg; w2 < wg + wpj; ++w2) {
+                                const float2 e = xm[(w2 * 2 + u) * 128 + rl];
+                                ll += e.y * ex2(e.x - mm);
+                            }
+                        part[(size_t)(j * 128 + rl) * ui.y] = make_float2(mm, ll);
                     }
                 }
+                named_bar_sync(1, kEpiThreads);
+            } else {
+                int u = 0;
+                for (int j = jfirst; j < J; j += jstep, ++u)
+                    part[(size_t)(j * 128 + rl) * ui.y] = u ? make_float2(m1, l1) : make_float2(m0, l0);
             }
-            __threadfence();
-            named_bar_sync(1, 256);
-            if (et == 0) {
-                const int2 ui = P.unit_items[I.unit];
-                const int prev = atomicAdd(P.unit_done + I.unit, 1);
-                *S.last_flag = (prev == ui.y - 1);
-            }
-            named_bar_sync(1, 256);
-            if (*S.last_flag) {
-                // last finisher of the unit: fold the partials in item order into c = m + log2(l)
-                __threadfence();
-                const int2 ui = P.unit_items[I.unit];
-                for (int row = et; row < P.slab_rows; row += 256) {
-                    float mm = -INFINITY;
-                    for (int p = 0; p < ui.y; ++p) mm = fmaxf(mm, __ldcg(&P.ml[(size_t)(ui.x + p) * P.slab_rows + row].x));
-                    float ll = 0.f;
-                    if (mm > -INFINITY) {
-                        for (int p = 0; p < ui.y; ++p) {
-                            const float2 e = __ldcg(&P.ml[(size_t)(ui.x + p) * P.slab_rows + row]);
-                            ll += e.y * ex2(e.x - mm);
-                        }
-                    }
-                    P.cvec[(size_t)I.unit * P.slab_rows + row] = mm == -INFINITY ? INFINITY : mm + log2f(ll);
-                }
-            }
-            named_bar_sync(1, 256);
         }
+    }
+}
+
+// Fold each query row's pass-1 partials (one per work item of its unit, in item order) into
+// c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
+__global__ void __launch_bounds__(256) merge_kernel(Params P) {
+    if (__ldcg(P.n_items + 1) == 0) return;
+    const int lane = threadIdx.x & 31;
+    const int64_t rows_all = (int64_t)P.R * P.units_per_req * P.slab_rows;
+    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
+    for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < rows_all; gr += wstride) {
+        const int u = static_cast<int>(gr / P.slab_rows), row = static_cast<int>(gr % P.slab_rows);
+        const int2 ui = P.unit_items[u];
+        const float2* part = P.ml + (size_t)ui.x * P.slab_rows + (size_t)row * ui.y;
+        float mm = -INFINITY;
+        for (int p = lane; p < ui.y; p += 32) mm = fmaxf(mm, __ldcg(&part[p].x));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
+        float ll = 0.f;
+        if (mm > -INFINITY)
+            for (int p = lane; p < ui.y; p += 32) {
+                const float2 e = __ldcg(&part[p]);
+                ll += e.y * ex2(e.x - mm);
+            }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
+        if (lane == 0) P.cvec[(size_t)u * P.slab_rows + row] = mm == -INFINITY ? INFINITY : mm + log2f(ll);
     }
 }
 
@@ -624,13 +788,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(S.tfull + b), 1);
-            mbar_init(smem_u32(S.tempty + b), 8);      // one arrival per epilogue warp
+            // one arrival per epilogue warp that reads the job: 4 warps per warpgroup on it
+            mbar_init(smem_u32(S.tempty + b), 4 * wg_per_job(P.J));
         }
         mbar_init(smem_u32(S.slab_full), 1);
         mbar_init(smem_u32(S.slab_free), 1);
         mbar_init(smem_u32(S.mma_done), 1);
         *S.abort_flag = 0;
-        *S.last_flag = 0;
         fence_mbar_init();
     }
     if (warp == 0 && lane == 0) {
@@ -647,18 +811,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem_base = *S.tmem_holder;
+    const uint32_t tmem_base = static_cast<uint32_t>(uni(static_cast<int>(*S.tmem_holder)));
 
-    const int n_items = __ldcg(P.n_items);
+    const int n_items = uni(__ldcg(P.n_items));
     const int it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
     const int it1 = static_cast<int>((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
 
     if (warp == 0) {
-        if (lane == 0) producer<NC>(P, S, &tmQ, &tmK, it0, it1);
+        producer<NC>(P, S, &tmQ, &tmK, it0, it1);
     } else if (warp == 1) {
-        if (lane == 0) mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1);
+        mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1);
     } else {
-        epilogue<PASS>(P, S, tmem_base, it0, it1);
+        switch (chunks_per_slice(P.J)) {         // 16-column chunks per job slice
+            case 8: epilogue<PASS, 8>(P, S, tmem_base, it0, it1); break;
+            case 4: epilogue<PASS, 4>(P, S, tmem_base, it0, it1); break;
+            default: epilogue<PASS, 2>(P, S, tmem_base, it0, it1); break;
+        }
     }
 
     tc_fence_before();
@@ -685,14 +853,14 @@ __device__ __forceinline__ int find_segment(const int32_t* cuts, int R, int x) {
 
 __global__ void finalize_kernel(Params P) {
     if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
-    const int units = P.units_per_req;
+    const int parts = P.units_per_req * 4;       // (unit, warpgroup) partials, summed in a fixed order
     const int nb_total = P.cb[P.R];
     const int stride = gridDim.x * blockDim.x;
     for (int gb = blockIdx.x * blockDim.x + threadIdx.x; gb < nb_total; gb += stride) {
         const int r = find_segment(P.cb, P.R, gb);
         const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
         float s = 0.f;
-        for (int kk = 0; kk < units; ++kk) s += P.blk[(size_t)kk * P.nb_cap + gb];
+        for (int kk = 0; kk < parts; ++kk) s += P.blk[(size_t)kk * P.nb_cap + gb];
         P.block_scores[gb] = s * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
     }
     if (P.token_scores != nullptr) {
@@ -700,7 +868,7 @@ __global__ void finalize_kernel(Params P) {
             const int r = find_segment(P.cu, P.R, t);
             const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
             float s = 0.f;
-            for (int kk = 0; kk < units; ++kk) s += P.tok[(size_t)kk * P.T + t];
+            for (int kk = 0; kk < parts; ++kk) s += P.tok[(size_t)kk * P.T + t];
             P.token_scores[t] = s * (1.0f / (static_cast<float>(ne) * P.Hq));
         }
     }
@@ -757,9 +925,13 @@ static cudaError_t launch_pass(const CUtensorMap& q, const CUtensorMap& k, const
 
 template <int NC>
 static cudaError_t launch_both(const CUtensorMap& q, const CUtensorMap& k, const Params& P, int grid,
-                               cudaStream_t st) {
+                               int64_t merge_rows, cudaStream_t st) {
     cudaError_t e = launch_pass<1, NC>(q, k, P, grid, st);
     if (e != cudaSuccess) return e;
+    const int mgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(merge_rows, 8), 16 * num_sms())));
+    merge_kernel<<<mgrid, 256, 0, st>>>(P);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
     return launch_pass<2, NC>(q, k, P, grid, st);
 }
 
@@ -821,7 +993,6 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.items = reinterpret_cast<int4*>(w + L.items);
     P.unit_items = reinterpret_cast<int2*>(w + L.unit_items);
     P.n_items = reinterpret_cast<int*>(w + L.n_items);
-    P.unit_done = reinterpret_cast<int*>(w + L.unit_done);
     P.ml = reinterpret_cast<float2*>(w + L.ml);
     P.cvec = reinterpret_cast<float*>(w + L.cvec);
     P.blk = reinterpret_cast<float*>(w + L.blk);
@@ -838,10 +1009,11 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
         if (!make_map(&tq, Q, T, Hq, dk, g.box_rows) || !make_map(&tk, K, T, Hkv, dk, kTileKeys)) return UP_ERR_CUDA;
         const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items_cap)));
         cudaError_t e;
+        const int64_t merge_rows = L.units * g.slab_rows;
         switch (g.nc) {
-            case 1: e = launch_both<1>(tq, tk, P, grid, st); break;
-            case 2: e = launch_both<2>(tq, tk, P, grid, st); break;
-            default: e = launch_both<4>(tq, tk, P, grid, st); break;
+            case 1: e = launch_both<1>(tq, tk, P, grid, merge_rows, st); break;
+            case 2: e = launch_both<2>(tq, tk, P, grid, merge_rows, st); break;
+            default: e = launch_both<4>(tq, tk, P, grid, merge_rows, st); break;
         }
         if (e != cudaSuccess) return UP_ERR_CUDA;
     }

@@ -6,9 +6,10 @@
 // One CTA per request, everything in shared memory, no CPU round trip:
 //   1. key_g = (phi(b_g) << 32) | g for the request's blocks (phi(x) = bits(x) ^ 0x80000000 for
 //      x >= 0; scores are non-negative sums of probabilities, so the sign bit decides phi).
-//   2. LSD radix sort of the 64-bit keys, descending, 4-bit digits, stable: the low word holds g
-//      (< 2^16), so only its low 16 bits and the 32 high bits carry information; digit passes
-//      above the block-index range are identity permutations and are skipped.
+//   2. LSD radix sort of the 64-bit keys, descending, 8-bit digits, stable.  The keys are laid out
+//      in descending order of g before the first pass, which is exactly the order the passes over
+//      the low (index) word would produce, so only the four passes over the high word run.  The
+//      result is the descending order of the packed 64-bit keys.
 //   3. inclusive prefix sum of the sorted scores in fp64 (fixed tree), k* = 1 + #{k : cum_k < p*total}.
 //   4. ranked flags by block index, then the byte masks: block(i) ranked, or i < A, or i >= N - n.
 #include <stdint.h>
@@ -19,8 +20,9 @@ namespace up {
 namespace select {
 
 constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 constexpr int kMaxIpt = UP_MAX_BLOCKS_PER_REQUEST / kThreads;   // 16 keys per thread
-constexpr int kDigits = 16;
+constexpr int kRadix = 256;
 
 __device__ __forceinline__ uint64_t pack_key(float b, uint32_t g) {
     const uint32_t bits = __float_as_uint(b);
@@ -68,14 +70,14 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     extern __shared__ __align__(16) uint8_t sm[];
     uint64_t* keys = reinterpret_cast<uint64_t*>(sm);                              // [8192]
     uint64_t* alt = keys + UP_MAX_BLOCKS_PER_REQUEST;                              // [8192]
-    uint32_t* cnt = reinterpret_cast<uint32_t*>(alt + UP_MAX_BLOCKS_PER_REQUEST);  // [16][512]
-    uint8_t* ranked = reinterpret_cast<uint8_t*>(cnt + kDigits * kThreads);        // [8192]
+    uint32_t* hist = reinterpret_cast<uint32_t*>(alt + UP_MAX_BLOCKS_PER_REQUEST); // [256 digits][16 warps]
+    uint8_t* ranked = reinterpret_cast<uint8_t*>(hist + kRadix * kWarps);          // [8192]
     __shared__ double shd[65];
     __shared__ int shi[65];
     __shared__ double s_total;
     __shared__ int s_bad;
 
-    const int r = blockIdx.x, tid = threadIdx.x;
+    const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c0 = cu[r], c1 = cu[r + 1];
     const int N = c1 - c0;
     const int nb = N > 0 ? (N + G - 1) / G : 0;
@@ -94,60 +96,67 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
         return;
     }
     const int b0 = cb[r];
-    const int ipt = (nb + kThreads - 1) / kThreads;      // keys per thread, contiguous
-    const int k0 = tid * ipt;
+    const int ipt = (nb + kThreads - 1) / kThreads;      // keys per thread
+    const int npad = ipt * kThreads;
 
-    // 1. packed keys (padding slots get key 0, which sorts last)
-    for (int j = 0; j < ipt; ++j) {
-        const int k = k0 + j;
-        keys[k] = k < nb ? pack_key(bs[b0 + k], static_cast<uint32_t>(k)) : 0ull;
+    // 1. packed keys, position k holds block g = nb-1-k (padding slots get key 0, which sorts last)
+    for (int k = tid; k < npad; k += kThreads) {
+        const int g = nb - 1 - k;
+        keys[k] = g >= 0 ? pack_key(bs[b0 + g], static_cast<uint32_t>(g)) : 0ull;
     }
     __syncthreads();
 
-    // 2. LSD radix sort, descending = ascending on ~key
-    int idx_bits = 0;
-    while ((1 << idx_bits) < nb) idx_bits += 4;
-    const int npass = idx_bits / 4 + 8;
-    for (int ps = 0; ps < npass; ++ps) {
-        const int shift = ps < idx_bits / 4 ? 4 * ps : 32 + 4 * (ps - idx_bits / 4);
-#pragma unroll
-        for (int d = 0; d < kDigits; ++d) cnt[d * kThreads + tid] = 0;
+    // 2. four stable passes over the high word, ascending on ~key (= descending on key).  Warp w owns
+    //    positions [w*32*ipt, (w+1)*32*ipt), visited round by round (32 consecutive keys per round), so
+    //    (digit, warp, round, lane) order equals (digit, position) order: the passes are stable.
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int ps = 0; ps < 4; ++ps) {
+        const int shift = 32 + 8 * ps;
+        for (int i = tid; i < kRadix * kWarps; i += kThreads) hist[i] = 0;
+        __syncthreads();
         uint32_t rank[kMaxIpt];
         uint32_t dig[kMaxIpt];
+        const int base_k = warp * 32 * ipt + lane;
 #pragma unroll
         for (int j = 0; j < kMaxIpt; ++j) {
             if (j < ipt) {
-                const uint32_t d = static_cast<uint32_t>((~keys[k0 + j]) >> shift) & 15u;
+                const uint32_t d = static_cast<uint32_t>((~keys[base_k + 32 * j]) >> shift) & 0xFFu;
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                const uint32_t before = hist[d * kWarps + warp];
+                __syncwarp();
+                if ((peers & lt_mask) == 0) hist[d * kWarps + warp] = before + __popc(peers);
+                __syncwarp();
                 dig[j] = d;
-                rank[j] = cnt[d * kThreads + tid]++;
+                rank[j] = before + __popc(peers & lt_mask);
             }
         }
         __syncthreads();
-        // exclusive scan over cnt in (digit, thread) order: 16 consecutive entries per thread
-        uint32_t loc[kDigits];
+        // exclusive scan of hist in (digit, warp) order: 8 consecutive entries per thread
+        uint32_t loc[8];
         uint32_t sum = 0;
 #pragma unroll
-        for (int e = 0; e < kDigits; ++e) {
-            loc[e] = cnt[tid * kDigits + e];
+        for (int e = 0; e < 8; ++e) {
+            loc[e] = hist[tid * 8 + e];
             sum += loc[e];
         }
         int tot;
         uint32_t run = static_cast<uint32_t>(block_exclusive_scan<int>(static_cast<int>(sum), shi, &tot));
 #pragma unroll
-        for (int e = 0; e < kDigits; ++e) {
+        for (int e = 0; e < 8; ++e) {
             const uint32_t c = loc[e];
-            cnt[tid * kDigits + e] = run;
+            hist[tid * 8 + e] = run;
             run += c;
         }
         __syncthreads();
 #pragma unroll
         for (int j = 0; j < kMaxIpt; ++j)
-            if (j < ipt) alt[cnt[dig[j] * kThreads + tid] + rank[j]] = keys[k0 + j];
+            if (j < ipt) alt[hist[dig[j] * kWarps + warp] + rank[j]] = keys[base_k + 32 * j];
         __syncthreads();
         uint64_t* t = keys;
         keys = alt;
         alt = t;
     }
+    const int k0 = tid * ipt;      // from here on each thread owns a contiguous run of sorted positions
 
     // 3. prefix sums of the sorted scores in fp64 and k*; the threshold uses the last prefix sum
     auto score_of = [&](int k) {
@@ -189,14 +198,27 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
         const bool forced = (static_cast<int64_t>(g) * G < A) || (static_cast<int64_t>(g + 1) * G > static_cast<int64_t>(N) - n);
         block_keep[b0 + g] = (ranked[g] || forced) ? 1 : 0;
     }
-    for (int i = tid; i < N; i += kThreads) {
-        const bool keep = ranked[i / G] || i < A || i >= N - n;
-        token_keep[c0 + i] = keep ? 1 : 0;
+    // token mask: byte i of the request is ranked[i >> log2 G] or a sink (i < A) or window (i >= N - n);
+    // the aligned interior is written 16 bytes per store, the unaligned head and tail byte by byte
+    const int gshift = __ffs(G) - 1;
+    auto keep_byte = [&](int i) -> uint32_t { return (ranked[i >> gshift] || i < A || i >= N - n) ? 1u : 0u; };
+    const int64_t a0 = c0, a1 = (int64_t)c0 + N;
+    const int64_t v0 = min((a0 + 15) & ~int64_t(15), a1), v1 = max(a1 & ~int64_t(15), v0);
+    for (int64_t t = a0 + tid; t < v0; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    for (int64_t t = v1 + tid; t < a1; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    for (int64_t t = v0 + 16 * (int64_t)tid; t < v1; t += 16 * (int64_t)kThreads) {
+        const int i0 = static_cast<int>(t - a0);
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = keep_byte(i0 + 4 * q) | (keep_byte(i0 + 4 * q + 1) << 8) | (keep_byte(i0 + 4 * q + 2) << 16) |
+                   (keep_byte(i0 + 4 * q + 3) << 24);
+        *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(w[0], w[1], w[2], w[3]);
     }
     if (tid == 0) kstar[r] = ks;
 }
 
-constexpr int kSmemBytes = 2 * UP_MAX_BLOCKS_PER_REQUEST * 8 + kDigits * kThreads * 4 + UP_MAX_BLOCKS_PER_REQUEST;
+constexpr int kSmemBytes = 2 * UP_MAX_BLOCKS_PER_REQUEST * 8 + kRadix * kWarps * 4 + UP_MAX_BLOCKS_PER_REQUEST;
 
 __global__ void __launch_bounds__(1024) cu_blocks_kernel(const int32_t* cu, int R, int T, int G, int32_t* cb,
                                                          int32_t* status) {
@@ -267,6 +289,7 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
         return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || nb_cap < 0 || G <= 0 || n < 1 || A < 0) return UP_ERR_ARG;
     if (!(p > 0.0) || !(p <= 1.0)) return UP_ERR_ARG;
+    if (G & (G - 1)) return UP_ERR_SHAPE;          // block size must be a power of two
     static int attr_done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return UP_ERR_CUDA;
