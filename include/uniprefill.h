@@ -151,6 +151,28 @@ up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seqlens, int R
                      int32_t* num_actual_tokens, int32_t* kept_len, uint8_t* drop_layer,
                      int L, int layer, void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
+/* up_compact without a workspace argument.  The paper has no counterpart: this entry point exists for
+ * callers that cannot allocate or lend device scratch memory (an engine whose memory planner owns all
+ * device memory after start-up, a plugin host that only passes the tensors it already holds, a loop
+ * that must avoid cudaMalloc's implicit synchronisation).  Arguments and results are those of
+ * up_compact, minus ws/ws_bytes.  Its per-tile counts and offsets live in a fixed array inside the
+ * library's device image (2 * (UP_NOALLOC_MAX_TOKENS / 1024 + 1) int32, about 128 KB), present on every
+ * GPU that loads the library until the process exits; the call allocates nothing.
+ *  - T > UP_NOALLOC_MAX_TOKENS returns UP_ERR_WORKSPACE before any launch (use up_compact instead).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ *    device current; make that first call before any stream capture.
+ *  - Every call on a device shares the one array and leaves its contents behind (nothing in it needs
+ *    clearing: each call overwrites what it reads).  Calls whose kernels can overlap on the GPU (for
+ *    example on two streams without ordering between them) race on it and give wrong results; order
+ *    them on one stream or use up_compact with separate workspaces. */
+#define UP_NOALLOC_MAX_TOKENS (16384 * 1024)
+up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t* cu_seqlens, int R, int64_t T,
+                             const uint16_t* hidden, int hdim, const int64_t* positions, const int64_t* slots,
+                             uint16_t* out_hidden, int64_t* out_positions, int64_t* out_slots,
+                             int32_t* kept_index, int32_t* new_cu_seqlens, int32_t* new_seq_lens,
+                             int32_t* num_actual_tokens, int32_t* kept_len, uint8_t* drop_layer,
+                             int L, int layer, int32_t* dev_status, void* stream);
+
 /* End-of-block carry-forward [UP 3.4, Eq. 8], in place:
  *   residual[kept_index[k], :] = new_states[k, :]  for k < *num_actual_tokens;
  *   rows of dropped tokens are not touched (they keep H^(b,0)).

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libuniprefill.so")
 
 UP_OK, UP_ERR_ARG, UP_ERR_SHAPE, UP_ERR_WORKSPACE, UP_ERR_CUDA, UP_ERR_DEVICE = range(6)
 MAX_BLOCKS_PER_REQUEST = 8192
+NOALLOC_MAX_TOKENS = 16384 * 1024
 
 _c_p = ctypes.c_void_p
 _i32, _i64, _f32, _f64, _sz, _u64 = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_double, ctypes.c_size_t, ctypes.c_uint64
@@ -37,6 +38,8 @@ _SIGNATURES = {
                                _c_p, _c_p, _c_p, _c_p, _c_p]),
     "up_compact": (_i32, [_c_p, _c_p, _i32, _i64, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                            _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _c_p, _sz, _c_p, _c_p]),
+    "up_compact_noalloc": (_i32, [_c_p, _c_p, _i32, _i64, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
+                                   _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _c_p, _c_p]),
     "up_scatter_back": (_i32, [_c_p, _c_p, _c_p, _i64, _i32, _c_p, _c_p, _c_p]),
     "up_slot_mapping": (_i32, [_c_p, _c_p, _i32, _i64, _c_p, _c_p, _i32, _i32, _c_p, _c_p, _c_p]),
     "up_seqused": (_i32, [_c_p, _c_p, _i32, _i32, _i32, _c_p, _c_p, _c_p, _c_p]),
@@ -155,6 +158,23 @@ def up_compact(token_keep, cu_seqlens, kept_index, new_cu_seqlens, new_seq_lens,
                                      _p(drop_layer), L, layer, _p(ws), ws.numel() * ws.element_size(),
                                      _p(dev_status), _stream(stream)),
            "up_compact")
+
+
+def up_compact_noalloc(token_keep, cu_seqlens, kept_index, new_cu_seqlens, new_seq_lens, num_actual_tokens,
+                       dev_status, hidden=None, out_hidden=None, positions=None, out_positions=None, slots=None,
+                       out_slots=None, kept_len=None, drop_layer=None, layer=0, stream=None):
+    """up_compact for callers that cannot provide a device workspace: the library's own fixed scratch
+    array is used instead (at most UP_NOALLOC_MAX_TOKENS tokens; calls that overlap on the GPU race)."""
+    R = cu_seqlens.numel() - 1
+    T = token_keep.numel()
+    hdim = hidden.shape[1] if hidden is not None else 0
+    L = drop_layer.numel() if drop_layer is not None else (kept_len.shape[0] if kept_len is not None else 0)
+    _check(load_library().up_compact_noalloc(_p(token_keep), _p(cu_seqlens), R, T, _p(hidden), hdim, _p(positions),
+                                             _p(slots), _p(out_hidden), _p(out_positions), _p(out_slots),
+                                             _p(kept_index), _p(new_cu_seqlens), _p(new_seq_lens),
+                                             _p(num_actual_tokens), _p(kept_len), _p(drop_layer), L, layer,
+                                             _p(dev_status), _stream(stream)),
+           "up_compact_noalloc")
 
 
 def up_scatter_back(new_states, kept_index, num_actual_tokens, residual, dev_status, stream=None):

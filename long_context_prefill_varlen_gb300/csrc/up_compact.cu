@@ -15,6 +15,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "up_internal.cuh"
 
@@ -298,5 +299,100 @@ extern "C" up_status up_scatter_back(const uint16_t* new_states, const int32_t* 
         reinterpret_cast<const uint4*>(new_states), reinterpret_cast<uint4*>(residual), kept_index, num_actual_tokens,
         T_upper, V, dev_status);
     count_launch();
+    return check_launch();
+}
+
+// ------------------------------------------------------------------------------------------------
+// Compaction without a caller workspace.
+//
+// Some callers cannot hand this library a scratch buffer: an inference engine whose memory planner
+// owns every byte of device memory after start-up, a plugin host that only passes in the tensors it
+// already has, or a latency-critical loop that must never hit cudaMalloc's implicit device
+// synchronisation.  For them up_compact_noalloc keeps the per-tile counts and offsets in a
+// fixed-size array that is part of this library's device image: it exists on every GPU that loads
+// the library, from load time until the process exits, and nothing is allocated per call.
+
+namespace up {
+namespace compact {
+
+constexpr int kNoAllocMaxTiles = UP_NOALLOC_MAX_TOKENS / kTile;        // 16384 tiles of 1024 tokens
+static_assert(UP_NOALLOC_MAX_TOKENS % kTile == 0, "the token limit must be whole tiles");
+
+// [0, kNoAllocMaxTiles + 1): tile counts; [kNoAllocMaxTiles + 1, 2 * (kNoAllocMaxTiles + 1)): offsets.
+// Every call overwrites every entry it reads, so nothing here needs clearing between calls.
+static __device__ __align__(256) int g_noalloc_scratch[2 * (kNoAllocMaxTiles + 1)];
+
+// Device address of g_noalloc_scratch on the current device (the host-side symbol is only a handle),
+// looked up once per device with that device current.
+static int* noalloc_scratch(up_status* err) {
+    static int* addr[64] = {nullptr};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = UP_ERR_CUDA;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+            *err = UP_ERR_CUDA;
+            return nullptr;
+        }
+        addr[dev] = static_cast<int*>(p);
+    }
+    *err = UP_OK;
+    return addr[dev];
+}
+
+}  // namespace compact
+}  // namespace up
+
+extern "C" up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t* cu_seqlens, int R, int64_t T,
+                                        const uint16_t* hidden, int hdim, const int64_t* positions,
+                                        const int64_t* slots, uint16_t* out_hidden, int64_t* out_positions,
+                                        int64_t* out_slots, int32_t* kept_index, int32_t* new_cu_seqlens,
+                                        int32_t* new_seq_lens, int32_t* num_actual_tokens, int32_t* kept_len,
+                                        uint8_t* drop_layer, int L, int layer, int32_t* dev_status, void* stream) {
+    if (!token_keep || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens || !num_actual_tokens ||
+        !dev_status)
+        return UP_ERR_ARG;
+    if (R <= 0 || T < 0 || T >= (int64_t(1) << 31)) return UP_ERR_ARG;
+    if (T > UP_NOALLOC_MAX_TOKENS) return UP_ERR_WORKSPACE;     // beyond the fixed scratch: use up_compact
+    if ((hidden == nullptr) != (out_hidden == nullptr) || (positions == nullptr) != (out_positions == nullptr) ||
+        (slots == nullptr) != (out_slots == nullptr))
+        return UP_ERR_ARG;
+    if ((kept_len || drop_layer) && (layer < 0 || layer >= L)) return UP_ERR_ARG;
+    if (hidden && (hdim <= 0 || hdim % 8 != 0 || !aligned16(hidden) || !aligned16(out_hidden))) return UP_ERR_SHAPE;
+    if (!aligned16(token_keep)) return UP_ERR_SHAPE;
+    up_status err;
+    int* scratch = compact::noalloc_scratch(&err);
+    if (scratch == nullptr) return err;
+    int* tile_cnt = scratch;
+    int* tile_off = scratch + compact::kNoAllocMaxTiles + 1;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int tiles = static_cast<int>(cdiv(T, compact::kTile));
+    const int Ti = static_cast<int>(T);
+    if (tiles > 0) {
+        compact::count_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_cnt);
+        count_launch();
+    }
+    compact::scan_kernel<<<1, 1024, 0, st>>>(token_keep, cu_seqlens, R, Ti, tile_cnt, tile_off, new_cu_seqlens,
+                                             new_seq_lens, num_actual_tokens, kept_len, drop_layer, layer,
+                                             dev_status);
+    count_launch();
+    if (tiles > 0) {
+        compact::index_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_off, positions, slots,
+                                                                      kept_index, out_positions, out_slots);
+        count_launch();
+        if (hidden) {
+            const int V = hdim / 8;
+            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T, compact::kRowThreads / 32), 4 * num_sms()));
+            compact::rows_kernel<true><<<grid, compact::kRowThreads, 0, st>>>(
+                reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), kept_index,
+                num_actual_tokens, T, V, dev_status);
+            count_launch();
+        }
+    }
     return check_launch();
 }
