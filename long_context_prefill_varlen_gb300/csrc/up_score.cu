@@ -16,14 +16,15 @@
 //
 // CTA layout (576 threads, one CTA per SM, persistent over a contiguous range of work items):
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 1     TMEM allocator and tcgen05.mma issuer
+//              (both run their loop on the whole warp and issue from one elected lane)
 //   warps 2-17 four epilogue warpgroups.  A job is one 128x128 fp32 accumulator; with J jobs per
 //              key tile, warpgroup g takes jobs g, g+4, ... when J >= 3, half a job (64 columns) when
 //              J = 2 and a quarter (32 columns) when J = 1.  TMEM is read in 16-column chunks, the
 //              next chunk's load in flight while the current one is reduced.
 // TMEM: 4 accumulators of 128 columns (the whole 512-column TMEM), used as a ring of jobs.
 // Per element the epilogue spends one ex2 on the SFU (32/clk/SM on this part, the same rate at
-// which the tensor core produces S elements at d_k = 128) plus packed f32x2 FMA/add work.
+// which the tensor core produces S elements at d_k = 128) plus one FFMA and one FADD.
 #include <math.h>
 
 #include <algorithm>
