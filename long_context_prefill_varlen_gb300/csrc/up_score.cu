@@ -14,10 +14,10 @@
 //   final   b_g = (sum over units of the partials) / (n_eff * Hq * G).
 // a = sm_scale * log2(e): the softmax is computed in base 2, exactly equal to exp in base e.
 //
-// CTA layout (576 threads, one CTA per SM, persistent over a contiguous range of work items):
+// CTA layout (608 threads, one CTA per SM, persistent over a contiguous range of work items):
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warp 1     TMEM allocator and tcgen05.mma issuer
-//              (both run their loop on the whole warp and issue from one elected lane)
+//   warp 1     TMEM allocator and tcgen05.mma issuer of the even jobs; warp 18 issues the odd jobs
+//              (all three run their loop on the whole warp and issue from one elected lane)
 //   warps 2-17 four epilogue warpgroups.  A job is one 128x128 fp32 accumulator; with J jobs per
 //              key tile, warpgroup g takes jobs g, g+4, ... when J >= 3, half a job (64 columns) when
 //              J = 2 and a quarter (32 columns) when J = 1.  TMEM is read in 16-column chunks, the
@@ -41,7 +41,10 @@ constexpr int kStages = 5;
 constexpr int kSlabBytes = 128 * 1024;          // resident query rows of one unit
 constexpr int kItemTiles = 2;                   // key tiles per work item (pass-1 partial granularity)
 constexpr int kEpiThreads = 512;
-constexpr int kThreads = 64 + kEpiThreads;
+constexpr int kIssuers = 2;                     // MMA issuer warps (warps 1 and 18), jobs split by parity
+constexpr int kEpiWarp0 = 2;                    // epilogue warps 2..17
+constexpr int kIssuer1Warp = kEpiWarp0 + kEpiThreads / 32;
+constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
 constexpr int kMaxJ = 8;                        // 128-row jobs per slab (d_k = 64 -> 8)
 constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
@@ -217,7 +220,7 @@ struct Smem {
     uint64_t* tempty;      // [4]        accumulator drained by both warpgroups
     uint64_t* slab_full;
     uint64_t* slab_free;
-    uint64_t* mma_done;
+    uint64_t* mma_done;    // [kIssuers]
     uint32_t* tmem_holder;
     int* abort_flag;
     float* cvec;           // [kCvecFloats]
@@ -238,7 +241,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.slab_full = b + 2 * kStages + 8;
     s.slab_free = b + 2 * kStages + 9;
     s.mma_done = b + 2 * kStages + 10;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(b + 2 * kStages + 11);
+    s.tmem_holder = reinterpret_cast<uint32_t*>(b + 2 * kStages + 10 + kIssuers);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
     s.cvec = reinterpret_cast<float*>(ctrl + kCtrlBytes);
     s.xchg = reinterpret_cast<uint8_t*>(s.cvec + kCvecFloats);
@@ -342,8 +345,16 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
 // the advance is a plain add on the descriptor.
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
+// Two issuer warps share the jobs by parity of the running job count: warp w issues job q iff
+// (q & 1) == w.  A tcgen05.commit holds up the thread that issues it until its earlier MMAs have
+// drained, and a single issuer that commits once per job leaves the tensor pipe idle for that
+// time (measured: 128x128x16 MMAs at ~96 instead of 64 cycles); with two issuers one warp's
+// commit overlaps the other's MMAs.  A commit tracks only its own thread's MMAs, so every barrier
+// that releases an operand (K stage, query slab) takes one commit from each issuer, and each
+// issuer waits for a stage to land before it commits the stage's release, even when it issued no
+// job on that tile: its arrival can then never count toward a later use of the stage.
 template <int PASS, int NC>
-__device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
+__device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1, uint32_t w) {
     volatile int* abort_flag = S.abort_flag;
     int prev_unit = -1;
     uint32_t stage_cnt = 0, slab_cnt = 0, jc = 0;
@@ -362,6 +373,7 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
         if (leader) tc_commit(bar);
         __syncwarp();
     };
+    auto mine = [&](uint32_t q) { return (q & 1u) == w; };
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
         if (I.unit != prev_unit) {
@@ -374,16 +386,18 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
         for (int kt = I.tb; kt < I.te; ++kt) {
             if (NC <= 2) {
                 // jobs outer: the tile's K stages stay resident while the J jobs run
+                bool landed = false;
                 for (int j = 0; j < J; ++j) {
-                    const uint32_t buf = jc & 3;
-                    if (!wait_all(smem_u32(S.tempty + buf), ((jc >> 2) & 1) ^ 1)) goto out;
+                    const uint32_t q = jc + j, buf = q & 3;
+                    if (!mine(q)) continue;
+                    if (!wait_all(smem_u32(S.tempty + buf), ((q >> 2) & 1) ^ 1)) goto out;
                     tc_fence_after();
                     const uint64_t qd = desc_add(slab_d0, j * 128 * 128);
                     const uint32_t d_tmem = tmem_base + buf * 128;
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
                         const uint32_t sc = stage_cnt + c, s = sc % kStages;
-                        if (j == 0) {
+                        if (!landed) {
                             if (!wait_all(smem_u32(S.full + s), (sc / kStages) & 1)) goto out;
                             tc_fence_after();
                         }
@@ -396,17 +410,22 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                             if (leader) tc_mma_bf16(d_tmem, a, b, kIdesc, (c | k) != 0);
                         }
                     }
+                    landed = true;
                     commit(smem_u32(S.tfull + buf));
-                    ++jc;
                 }
 #pragma unroll
-                for (int c = 0; c < NC; ++c) commit(smem_u32(S.empty + (stage_cnt + c) % kStages));
+                for (int c = 0; c < NC; ++c) {
+                    const uint32_t sc = stage_cnt + c;
+                    if (!landed && !wait_all(smem_u32(S.full + sc % kStages), (sc / kStages) & 1)) goto out;
+                    commit(smem_u32(S.empty + sc % kStages));
+                }
                 stage_cnt += NC;
+                jc += J;
             } else {
                 // chunks outer (d_k = 256, J <= 2): each K stage is released as soon as all jobs used it
                 for (int j = 0; j < J; ++j) {
                     const uint32_t q = jc + j;
-                    if (!wait_all(smem_u32(S.tempty + (q & 3)), ((q >> 2) & 1) ^ 1)) goto out;
+                    if (mine(q) && !wait_all(smem_u32(S.tempty + (q & 3)), ((q >> 2) & 1) ^ 1)) goto out;
                 }
                 tc_fence_after();
 #pragma unroll
@@ -416,6 +435,7 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                     tc_fence_after();
                     const uint64_t kd = desc_add(stage_d0, s * kStageBytes);
                     for (int j = 0; j < J; ++j) {
+                        if (!mine(jc + j)) continue;
                         const uint32_t d_tmem = tmem_base + ((jc + j) & 3) * 128;
                         const uint64_t qdc = desc_add(slab_d0, j * 128 * 128 + c * slab_chunk_bytes);
 #pragma unroll
@@ -428,17 +448,18 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                     commit(smem_u32(S.empty + s));
                     ++stage_cnt;
                 }
-                for (int j = 0; j < J; ++j) commit(smem_u32(S.tfull + ((jc + j) & 3)));
+                for (int j = 0; j < J; ++j)
+                    if (mine(jc + j)) commit(smem_u32(S.tfull + ((jc + j) & 3)));
                 jc += J;
             }
         }
     }
 out:
-    // make sure no MMA is still running when the CTA tears down its TMEM
+    // make sure none of this warp's MMAs is still running when the CTA tears down its TMEM
     __syncwarp();
-    commit(smem_u32(S.mma_done));
+    commit(smem_u32(S.mma_done + w));
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(smem_u32(S.mma_done), 0)) {
+    while (!mbar_try_wait(smem_u32(S.mma_done + w), 0)) {
         if (globaltimer_ns() - t0 > kWaitLimitNs) break;
     }
 }
@@ -482,6 +503,37 @@ __device__ __forceinline__ void tmem_wait_pin(uint32_t (&v)[16]) {
 
 __device__ __forceinline__ float f(uint32_t x) { return __uint_as_float(x); }
 
+// Packed fp32 pairs: the f32x2 forms of add and fma do the work of two scalar instructions in one
+// issue slot, each half rounded exactly as the scalar instruction rounds it.
+__device__ __forceinline__ uint64_t pk2(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ float2 up2(uint64_t x) {
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(x));
+    return r;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t x, uint64_t y, uint64_t z) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t x, uint64_t y) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+    return d;
+}
+__device__ __forceinline__ uint64_t ex2_2(uint64_t x) {     // 2^x of both halves, on the SFU
+    const float2 t = up2(x);
+    return pk2(ex2(t.x), ex2(t.y));
+}
+// 2^(S*a + z) for the element pair (v[c], v[c+1])
+__device__ __forceinline__ uint64_t p2(const uint32_t (&v)[16], int c, uint64_t a2, uint64_t z2) {
+    return ex2_2(fma2(pk2(f(v[c]), f(v[c + 1])), a2, z2));
+}
+
 // pass 1, one 16-column chunk of one query row, every column visible: online (m, l) in base 2,
 // m = max S*a, l = sum 2^(S*a - m); the running sum is rescaled only when the max grows
 __device__ __forceinline__ void row_chunk_full(const uint32_t (&v)[16], float a, float& m, float& l) {
@@ -493,16 +545,15 @@ __device__ __forceinline__ void row_chunk_full(const uint32_t (&v)[16], float a,
         l *= ex2(m - mx);
         m = mx;
     }
-    const float nm = -m;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+    const uint64_t a2 = pk2(a, a), nm2 = pk2(-m, -m);
+    uint64_t s0 = p2(v, 0, a2, nm2), s1 = p2(v, 2, a2, nm2);
 #pragma unroll
-    for (int c = 0; c < 16; c += 4) {
-        s0 += ex2(fmaf(f(v[c]), a, nm));
-        s1 += ex2(fmaf(f(v[c + 1]), a, nm));
-        s2 += ex2(fmaf(f(v[c + 2]), a, nm));
-        s3 += ex2(fmaf(f(v[c + 3]), a, nm));
+    for (int c = 4; c < 16; c += 4) {
+        s0 = add2(s0, p2(v, c, a2, nm2));
+        s1 = add2(s1, p2(v, c + 2, a2, nm2));
     }
-    l += (s0 + s1) + (s2 + s3);
+    const float2 t = up2(add2(s0, s1));
+    l += t.x + t.y;
 }
 
 // pass 1 with the causal limit: columns c <= lim are visible
@@ -525,31 +576,34 @@ __device__ __forceinline__ void row_chunk_masked(const uint32_t (&v)[16], int li
 }
 
 // pass 2, one 16-column chunk of one key, every row visible: sum of 2^(S*a - c_row); ncv holds -c_row
-// (-inf for rows that are not window rows of this request, which therefore contribute 0)
-__device__ __forceinline__ void key_chunk_full(const uint32_t (&v)[16], const float* ncv, float a, float (&acc)[4]) {
+// (-inf for rows that are not window rows of this request, which therefore contribute 0).  The sum
+// is kept as two packed pairs.
+__device__ __forceinline__ void key_chunk_full(const uint32_t (&v)[16], const float* ncv, float a, uint64_t (&acc)[2]) {
     const float4* nc4 = reinterpret_cast<const float4*>(ncv);
+    const uint64_t a2 = pk2(a, a);
 #pragma unroll
     for (int c = 0; c < 16; c += 4) {
         const float4 n = nc4[c / 4];
-        acc[0] += ex2(fmaf(f(v[c]), a, n.x));
-        acc[1] += ex2(fmaf(f(v[c + 1]), a, n.y));
-        acc[2] += ex2(fmaf(f(v[c + 2]), a, n.z));
-        acc[3] += ex2(fmaf(f(v[c + 3]), a, n.w));
+        acc[0] = add2(acc[0], p2(v, c, a2, pk2(n.x, n.y)));
+        acc[1] = add2(acc[1], p2(v, c + 2, a2, pk2(n.z, n.w)));
     }
 }
 
 // pass 2 with the causal mask: key i is visible to the query row at local position pos iff i <= pos
 __device__ __forceinline__ void key_chunk_masked(const uint32_t (&v)[16], const float* ncv, float a, int i, int qg0,
-                                                 int n, int N, int rows_total, float (&acc)[4]) {
+                                                 int n, int N, int rows_total, uint64_t (&acc)[2]) {
     if (i >= N) return;
+    float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
         const int qg = qg0 + c;
         const int pos = N - n + (qg % n);
         const bool vis = qg < rows_total && pos >= 0 && i <= pos;
         const float p = ex2(fmaf(f(v[c]), a, ncv[c]));
-        acc[c & 3] += vis ? p : 0.f;
+        s[c & 3] += vis ? p : 0.f;
     }
+    acc[0] = add2(acc[0], pk2(s[0], s[1]));
+    acc[1] = add2(acc[1], pk2(s[2], s[3]));
 }
 
 __device__ __forceinline__ void release_tmem(const Smem& S, uint32_t buf, int lane) {
@@ -558,43 +612,38 @@ __device__ __forceinline__ void release_tmem(const Smem& S, uint32_t buf, int la
     if (lane == 0) mbar_arrive(smem_u32(S.tempty + buf));
 }
 
-struct JobCtx {
-    float a;
-    int lim0;          // pass 1: last visible column of the job slice (relative to its first column)
-    bool rvalid;       // pass 1: this thread's row is a window row of the request
-    bool fast;         // every element of the job slice is visible to this thread
-    int key, qg0, n, N, rows_total;
-    const float* ncv0;
-};
-
 // One job slice whose every element is visible to every thread of the warp: NCH 16-column chunks,
 // TMEM loads double-buffered (the next chunk in flight while the current one is reduced); the TMEM
 // buffer is released as soon as its last chunk has landed.  Straight-line code, kept compact.
+// Pass 1 updates (m, l) of this thread's row; pass 2 adds into this thread's key sum.
 template <int PASS, int NCH>
-__device__ __forceinline__ void run_job_fast(const Smem& S, uint32_t ta, uint32_t buf, int lane, const JobCtx& c,
-                                             float& m, float& l, float (&acc)[4]) {
+__device__ __forceinline__ void run_job_fast(const Smem& S, uint32_t ta, uint32_t buf, int lane, float a,
+                                             const float* ncv0, float& m, float& l, uint64_t (&acc)[2]) {
     uint32_t va[16], vb[16];
     tmem_ld16(ta, va);
     tmem_wait_pin(va);
 #pragma unroll
     for (int ch = 0; ch < NCH; ch += 2) {
         tmem_ld16(ta + (ch + 1) * 16, vb);
-        if (PASS == 1) row_chunk_full(va, c.a, m, l);
-        else key_chunk_full(va, c.ncv0 + ch * 16, c.a, acc);
+        if (PASS == 1) row_chunk_full(va, a, m, l);
+        else key_chunk_full(va, ncv0 + ch * 16, a, acc);
         tmem_wait_pin(vb);
         if (ch + 2 < NCH) tmem_ld16(ta + (ch + 2) * 16, va);
         else release_tmem(S, buf, lane);
-        if (PASS == 1) row_chunk_full(vb, c.a, m, l);
-        else key_chunk_full(vb, c.ncv0 + (ch + 1) * 16, c.a, acc);
+        if (PASS == 1) row_chunk_full(vb, a, m, l);
+        else key_chunk_full(vb, ncv0 + (ch + 1) * 16, a, acc);
         if (ch + 2 < NCH) tmem_wait_pin(va);
     }
 }
 
 // The general case (tiles that reach into the causal window or past the request's end, and the
-// abort path): one chunk at a time with the masks; rare, so kept out of the fast path's code.
+// abort path, which reads nothing and only releases the buffer): one chunk at a time with the masks.
+// Pass 1: columns up to lim0 (relative to the slice's first column) of a valid row; pass 2: key
+// `key` against the slice's rows qg0.. of a request of N tokens.
 template <int PASS>
-__device__ __noinline__ void run_job_slow(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool ok, int nch,
-                                          const JobCtx& c, float& m, float& l, float (&acc)[4]) {
+__device__ __forceinline__ void run_job_slow(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool ok, int nch,
+                                             float a, bool rvalid, int lim0, const float* ncv0, int key, int qg0,
+                                             int n, int N, int rows_total, float& m, float& l, uint64_t (&acc)[2]) {
     for (int ch = 0; ch < nch; ++ch) {
         uint32_t v[16];
         if (ok) {
@@ -605,10 +654,11 @@ __device__ __noinline__ void run_job_slow(const Smem& S, uint32_t ta, uint32_t b
             for (int i = 0; i < 16; ++i) v[i] = 0u;
         }
         if (ch == nch - 1) release_tmem(S, buf, lane);
+        if (!ok) continue;
         if (PASS == 1) {
-            if (c.rvalid) row_chunk_masked(v, c.lim0 - ch * 16, c.a, m, l);
+            if (rvalid) row_chunk_masked(v, lim0 - ch * 16, a, m, l);
         } else {
-            key_chunk_masked(v, c.ncv0 + ch * 16, c.a, c.key, c.qg0 + ch * 16, c.n, c.N, c.rows_total, acc);
+            key_chunk_masked(v, ncv0 + ch * 16, a, key, qg0 + ch * 16, n, N, rows_total, acc);
         }
     }
 }
@@ -630,9 +680,13 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
     const int jstep = 4 / wpj;
     const uint32_t tl = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + col0;
     uint32_t tiles_done = 0;
-    int prev_unit = -1;
+    int prev_unit = -1, prev_slab = -1;
     uint32_t tile_par = 0;
     float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;   // pass 1 state of the (<= 2) jobs
+    // pass 1: this thread's row in each of its (<= 2) jobs: inside the slab's rows, and its position
+    // in the window (qg % n); set when the slab changes
+    bool rin0 = false, rin1 = false;
+    int rmod0 = 0, rmod1 = 0;
 
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
@@ -645,12 +699,20 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
             named_bar_sync(1, kEpiThreads);
         }
         prev_unit = I.unit;
+        if (PASS == 1 && I.slab != prev_slab) {
+            const int q0 = row0 + jfirst * 128 + rl, q1 = q0 + jstep * 128;
+            rin0 = jfirst < J && q0 < P.rows_total;
+            rin1 = jfirst + jstep < J && q1 < P.rows_total;
+            rmod0 = q0 % P.n;
+            rmod1 = q1 % P.n;
+            prev_slab = I.slab;
+        }
         if (PASS == 1) {
             m0 = m1 = -INFINITY;
             l0 = l1 = 0.f;
         }
         for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
+            uint64_t acc[2] = {0ull, 0ull};                 // pass 2: packed (+0.0f, +0.0f) pairs
             const bool tile_full = kt * kTileKeys + kTileKeys - 1 <= I.N - ne;
             int u = 0;
             for (int j = jfirst; j < J; j += jstep, ++u) {
@@ -659,24 +721,25 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                 const bool ok =
                     __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (jc >> 2) & 1, abort_flag));
                 tc_fence_after();
-                JobCtx c;
-                c.a = a;
-                const int qg_row = row0 + j * 128 + rl;                       // pass 1: this thread's row
-                const int pos_row = I.N - P.n + (qg_row % P.n);
-                c.rvalid = qg_row < P.rows_total && pos_row >= 0;
-                c.lim0 = pos_row - (kt * kTileKeys + col0);
-                c.key = kt * kTileKeys + rl;                                  // pass 2: this thread's key
-                c.qg0 = row0 + j * 128 + col0;
-                c.n = P.n;
-                c.N = I.N;
-                c.rows_total = P.rows_total;
-                c.ncv0 = S.cvec + j * 128 + col0;
-                c.fast = PASS == 1 ? (c.rvalid && c.lim0 >= cols - 1) : tile_full;
+                const uint32_t ta = tl + buf * 128;
+                const float* ncv0 = S.cvec + j * 128 + col0;
                 float mm = u ? m1 : m0, ll = u ? l1 : l0;
-                if (ok && __all_sync(0xffffffffu, c.fast))
-                    run_job_fast<PASS, NCH>(S, tl + buf * 128, buf, lane, c, mm, ll, acc);
+                bool rvalid = false;
+                int lim0 = 0;
+                bool fast;
+                if (PASS == 1) {
+                    const int pos = I.N - P.n + (u ? rmod1 : rmod0);    // this thread's row position
+                    rvalid = (u ? rin1 : rin0) && pos >= 0;
+                    lim0 = pos - (kt * kTileKeys + col0);               // last visible column of the slice
+                    fast = rvalid && lim0 >= cols - 1;
+                } else {
+                    fast = tile_full;
+                }
+                if (ok && __all_sync(0xffffffffu, fast))
+                    run_job_fast<PASS, NCH>(S, ta, buf, lane, a, ncv0, mm, ll, acc);
                 else
-                    run_job_slow<PASS>(S, tl + buf * 128, buf, lane, ok, NCH, c, mm, ll, acc);
+                    run_job_slow<PASS>(S, ta, buf, lane, ok, NCH, a, rvalid, lim0, ncv0, kt * kTileKeys + rl,
+                                       row0 + j * 128 + col0, P.n, I.N, P.rows_total, mm, ll, acc);
                 if (PASS == 1) {
                     if (u) { m1 = mm; l1 = ll; } else { m0 = mm; l0 = ll; }
                 }
@@ -684,7 +747,8 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
             if (PASS == 2) {
                 // this warpgroup's per-key partial, reduced over G consecutive keys (keys are TMEM lanes,
                 // so warp shuffles, then the warps of the group for G > 32); one partial per warpgroup
-                const float tot = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                const float2 t01 = up2(acc[0]), t23 = up2(acc[1]);
+                const float tot = (t01.x + t01.y) + (t23.x + t23.y);
                 const int i = kt * kTileKeys + rl;
                 const size_t part = (size_t)I.kk * 4 + wg;
                 if (P.tok != nullptr && i < I.N) P.tok[part * P.T + I.base + i] = tot;
@@ -785,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(smem_u32(S.full + s), 1);
-            mbar_init(smem_u32(S.empty + s), 1);
+            mbar_init(smem_u32(S.empty + s), kIssuers);    // one commit from each issuer
         }
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(S.tfull + b), 1);
@@ -793,8 +857,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(S.tempty + b), 4 * wg_per_job(P.J));
         }
         mbar_init(smem_u32(S.slab_full), 1);
-        mbar_init(smem_u32(S.slab_free), 1);
-        mbar_init(smem_u32(S.mma_done), 1);
+        mbar_init(smem_u32(S.slab_free), kIssuers);
+        for (int w = 0; w < kIssuers; ++w) mbar_init(smem_u32(S.mma_done + w), 1);
         *S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -820,8 +884,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         producer<NC>(P, S, &tmQ, &tmK, it0, it1);
-    } else if (warp == 1) {
-        mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1);
+    } else if (warp == 1 || warp == kIssuer1Warp) {
+        mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : 1u);
     } else {
         switch (chunks_per_slice(P.J)) {         // 16-column chunks per job slice
             case 8: epilogue<PASS, 8>(P, S, tmem_base, it0, it1); break;
