@@ -589,16 +589,20 @@ __device__ __forceinline__ void key_chunk_full(const uint32_t (&v)[16], const fl
     }
 }
 
-// pass 2 with the causal mask: key i is visible to the query row at local position pos iff i <= pos
+// pass 2 with the causal mask: key i is visible to the query row at local position pos iff i <= pos.
+// The slab's rows are head-major (row qg is window position qg % n of head qg / n) and qg0 and n are
+// multiples of 16, so the chunk's 16 rows are window positions t0 .. t0 + 15 of one head: one modulo
+// per chunk instead of one per element.
 __device__ __forceinline__ void key_chunk_masked(const uint32_t (&v)[16], const float* ncv, float a, int i, int qg0,
                                                  int n, int N, int rows_total, uint64_t (&acc)[2]) {
     if (i >= N) return;
+    const int t0 = qg0 % n;
+    const int lim = i - (N - n + t0);              // column c is visible iff c >= lim (pos = N - n + t0 + c >= i)
+    const int rows_left = rows_total - qg0;        // and c < rows_left
     float s[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-        const int qg = qg0 + c;
-        const int pos = N - n + (qg % n);
-        const bool vis = qg < rows_total && pos >= 0 && i <= pos;
+        const bool vis = c >= lim && c < rows_left && N - n + t0 + c >= 0;
         const float p = ex2(fmaf(f(v[c]), a, ncv[c]));
         s[c & 3] += vis ? p : 0.f;
     }
