@@ -827,16 +827,30 @@ __global__ void __launch_bounds__(256) merge_kernel(Params P) {
         const int u = static_cast<int>(gr / P.slab_rows), row = static_cast<int>(gr % P.slab_rows);
         const int2 ui = P.unit_items[u];
         const float2* part = P.ml + (size_t)ui.x * P.slab_rows + (size_t)row * ui.y;
+        // the first kCache partials of each lane stay in registers between the max and the sum (one
+        // round of loads instead of two); the sum keeps its order (p = lane, lane + 32, ...)
+        constexpr int kCache = 8;
+        float2 e[kCache];
         float mm = -INFINITY;
-        for (int p = lane; p < ui.y; p += 32) mm = fmaxf(mm, __ldcg(&part[p].x));
+#pragma unroll
+        for (int i = 0; i < kCache; ++i) {
+            const int p = lane + 32 * i;
+            e[i] = p < ui.y ? __ldcg(&part[p]) : make_float2(-INFINITY, 0.f);
+            mm = fmaxf(mm, e[i].x);
+        }
+        for (int p = lane + 32 * kCache; p < ui.y; p += 32) mm = fmaxf(mm, __ldcg(&part[p].x));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, o));
         float ll = 0.f;
-        if (mm > -INFINITY)
-            for (int p = lane; p < ui.y; p += 32) {
-                const float2 e = __ldcg(&part[p]);
-                ll += e.y * ex2(e.x - mm);
+        if (mm > -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < kCache; ++i)
+                if (e[i].x > -INFINITY) ll += e[i].y * ex2(e[i].x - mm);     // an empty partial adds 0
+            for (int p = lane + 32 * kCache; p < ui.y; p += 32) {
+                const float2 x = __ldcg(&part[p]);
+                ll += x.y * ex2(x.x - mm);
             }
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
         if (lane == 0) P.cvec[(size_t)u * P.slab_rows + row] = mm == -INFINITY ? INFINITY : mm + log2f(ll);
@@ -920,6 +934,21 @@ __device__ __forceinline__ int find_segment(const int32_t* cuts, int R, int x) {
     return lo;
 }
 
+// sum of parts values x[k * stride], k = 0, 1, ... in that order; the loads go out eight at a time
+__device__ __forceinline__ float sum_parts(const float* x, int64_t stride, int parts) {
+    float s = 0.f;
+    int k = 0;
+    for (; k + 8 <= parts; k += 8) {
+        float v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = __ldcg(x + (size_t)(k + i) * stride);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s += v[i];
+    }
+    for (; k < parts; ++k) s += __ldcg(x + (size_t)k * stride);
+    return s;
+}
+
 __global__ void finalize_kernel(Params P) {
     if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
     const int parts = P.units_per_req * 4;       // (unit, warpgroup) partials, summed in a fixed order
@@ -928,17 +957,13 @@ __global__ void finalize_kernel(Params P) {
     for (int gb = blockIdx.x * blockDim.x + threadIdx.x; gb < nb_total; gb += stride) {
         const int r = find_segment(P.cb, P.R, gb);
         const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
-        float s = 0.f;
-        for (int kk = 0; kk < parts; ++kk) s += P.blk[(size_t)kk * P.nb_cap + gb];
-        P.block_scores[gb] = s * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
+        P.block_scores[gb] = sum_parts(P.blk + gb, P.nb_cap, parts) * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
     }
     if (P.token_scores != nullptr) {
         for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < P.T; t += stride) {
             const int r = find_segment(P.cu, P.R, t);
             const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
-            float s = 0.f;
-            for (int kk = 0; kk < parts; ++kk) s += P.tok[(size_t)kk * P.T + t];
-            P.token_scores[t] = s * (1.0f / (static_cast<float>(ne) * P.Hq));
+            P.token_scores[t] = sum_parts(P.tok + t, P.T, parts) * (1.0f / (static_cast<float>(ne) * P.Hq));
         }
     }
 }
