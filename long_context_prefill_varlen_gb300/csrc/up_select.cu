@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     __shared__ int shi[65];
     __shared__ double s_total;
     __shared__ int s_bad;
+    __shared__ int s_below;
 
     const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c0 = cu[r], c1 = cu[r + 1];
@@ -184,9 +185,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
             below += run < thr;
         }
     }
-    int nbelow;
-    (void)block_exclusive_scan<int>(below, shi, &nbelow);
-    const int ks = min(nb, nbelow + 1);
+    if (tid == 0) s_below = 0;                     // #{k : cum_k < thr}: an integer count, any order
+    __syncthreads();
+    if (below) atomicAdd(&s_below, below);
+    __syncthreads();
+    const int ks = min(nb, s_below + 1);
 
     // 4. ranked flags by block index, then block and token masks
     for (int j = 0; j < ipt; ++j) {
@@ -206,8 +209,16 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     const int64_t v0 = min((a0 + 15) & ~int64_t(15), a1), v1 = max(a1 & ~int64_t(15), v0);
     for (int64_t t = a0 + tid; t < v0; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
     for (int64_t t = v1 + tid; t < a1; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    // with the request start 16-byte aligned and G >= 16, a 16-byte group lies in one block; clear
+    // of the sinks and the window it is that block's flag repeated
+    const bool whole = G >= 16 && v0 == a0;
     for (int64_t t = v0 + 16 * (int64_t)tid; t < v1; t += 16 * (int64_t)kThreads) {
         const int i0 = static_cast<int>(t - a0);
+        if (whole && i0 >= A && i0 + 15 < N - n) {
+            const uint32_t b = ranked[i0 >> gshift] ? 0x01010101u : 0u;
+            *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(b, b, b, b);
+            continue;
+        }
         uint32_t w[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
