@@ -8,7 +8,9 @@ value = tokens of the batch / device time of one step (CUDA events on the launch
 Default workload: LLaMA-3.1-8B full-attention layer, one request of 32768 tokens (32/8 heads,
 d_k 128, hidden 4096, G 64, n 128, A 128, p 0.99), synthetic seeded bf16 inputs.  L2 is
 flushed (512 MB write) before every timed step.  `--impl reference` times the fp64 CPU oracle
-on the host cores instead (bounded sample of the same workload per step).
+on the host cores instead (bounded sample of the same workload per step).  `--sweep rho|ablation`
+prints measured sweeps instead of the step line (compaction against the kept fraction; the stages
+over G, n and p).
 """
 from __future__ import annotations
 
@@ -42,6 +44,10 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--p", type=float, default=None, help="override the workload's top-p threshold")
+    ap.add_argument("--sweep", choices=["rho", "ablation"], default=None,
+                    help="instead of the step line, one JSON line per point: 'rho' = compaction and scatter "
+                         "bandwidth against the kept fraction; 'ablation' = the step's stages over G, n and p")
     return ap.parse_args()
 
 
@@ -321,6 +327,90 @@ def run_reference(args, w, rank, world):
             "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+# ------------------------------------------------------------------------------------------ sweeps
+
+def _time_events(fn, steps, flush, stream):
+    """mean device time (ms) of fn() over `steps` calls, L2 flushed before each, events on `stream`"""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        flush.fill_(1)
+        ev[k][0].record(stream)
+        fn()
+        ev[k][1].record(stream)
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev]))
+
+
+def run_sweep(args, w):
+    """Measured sweeps on the workload's geometry; one JSON line per point (not the step line)."""
+    import torch
+    import long_context_prefill_varlen_gb300 as up
+    from synth import gpu as sgpu
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    up.load_library()
+    stream = torch.cuda.current_stream()
+    pk, pk_kind = peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    steps = max(3, min(args.steps, 50))
+    if args.sweep == "rho":
+        # compaction gather and scatter-back against the kept fraction: whole G-token blocks kept with
+        # probability rho (seeded), the rest of the step not involved
+        inputs = sgpu.build_device(w, device=dev, parts=("hidden", "positions", "slots"))
+        cu = torch.tensor(w.cu_seqlens(), dtype=torch.int32, device=dev)
+        step = up.DropStep(cu, w.T, w.Hq, w.Hkv, w.dk, w.hdim, G=w.G, n=w.n, A=w.A, p=w.p, device=dev)
+        residual = inputs["hidden"].clone()
+        rng = np.random.default_rng(7)
+        nblk = -(-w.T // w.G)
+        for rho in (0.1, 0.25, 0.5, 0.75, 0.9, 0.99, 1.0):
+            blk = rng.random(nblk) < rho
+            keep = np.repeat(blk, w.G)[:w.T].astype(np.uint8)
+            step.token_keep.copy_(torch.from_numpy(keep).to(dev))
+            comp = lambda: step.compact(inputs["hidden"], inputs["positions"], inputs["slots"])
+            scat = lambda: step.scatter_back(step.out_hidden, residual)
+            for _ in range(3):
+                comp()
+                scat()
+            torch.cuda.synchronize()
+            step.check()
+            kept = int(step.num_actual.item())
+            cms = _time_events(comp, steps, flush, stream)
+            sms = _time_events(scat, steps, flush, stream)
+            rows = 2 * kept * w.hdim * 2 + kept * 4
+            print(json.dumps({"sweep": "rho", "workload": w.name, "rho": kept / w.T, "kept_tokens": kept,
+                              "compact_ms": cms, "compact_gbs": rows / (cms * 1e-3) / 1e9,
+                              "compact_frac_of_hbm": rows / (cms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                              "scatter_ms": sms, "scatter_gbs": rows / (sms * 1e-3) / 1e9,
+                              "scatter_frac_of_hbm": rows / (sms * 1e-3) / 1e9 / pk["hbm_gbs"],
+                              "steps": steps, "peak_source": pk_kind}), flush=True)
+        return
+    # ablation: G, n and p on the workload's geometry (the step's stages, eager, events between)
+    inputs = sgpu.build_device(w, device=dev)
+    cu = inputs["cu_seqlens"]
+    for G in (32, 64, 128):
+        for n in (32, 128, 512):
+            for p in (0.98, 0.99):
+                step = up.DropStep(cu, w.T, w.Hq, w.Hkv, w.dk, w.hdim, G=G, n=n, A=w.A, p=p, device=dev)
+                fns = [lambda: step.score(inputs["Q"], inputs["K"]), step.select,
+                       lambda: step.compact(inputs["hidden"], inputs["positions"], inputs["slots"])]
+                for _ in range(3):
+                    for f in fns:
+                        f()
+                torch.cuda.synchronize()
+                step.check()
+                ms = [_time_events(f, steps, flush, stream) for f in fns]
+                kept = int(step.num_actual.item())
+                wv = w.replace(G=G, n=n, p=p)
+                print(json.dumps({"sweep": "ablation", "workload": w.name, "G": G, "n": n, "p": p,
+                                  "rho": kept / w.T, "kstar": step.kstar.cpu().tolist()[:4],
+                                  "score_ms": ms[0], "select_ms": ms[1], "compact_ms": ms[2],
+                                  "score_frac_of_bf16_peak": score_flops(wv) / (ms[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
+                                  "select_share": ms[1] / sum(ms), "steps": steps}), flush=True)
+                del step
+                torch.cuda.empty_cache()
+
+
 # ------------------------------------------------------------------------------------------ report
 
 def workload_config(w):
@@ -349,6 +439,13 @@ def measured_traffic(kernel, w):
     return e["dram_bytes_per_launch"]
 
 
+def score_input_bytes(w):
+    """DRAM input of both passes: K once per pass, plus the window rows of Q once per (KV head) unit."""
+    kb = w.T * w.Hkv * w.dk * 2
+    qb = sum(min(w.n, N) for N in w.lengths) * w.Hq * w.dk * 2
+    return 2 * (kb + qb)
+
+
 def score_flops(w):
     """Algorithmic FLOPs of both passes: 2 * d_k * (n_eff*N - n_eff(n_eff-1)/2) per (request, query head, pass)."""
     tot = 0
@@ -371,6 +468,12 @@ def main():
             dist.init_process_group("nccl")
     from synth import recipe
     w = recipe.workload(args.config)
+    if args.p is not None:
+        w = w.replace(p=args.p)
+    if args.sweep is not None:
+        if rank == 0:
+            run_sweep(args, w)
+        return
     if args.impl == "reference":
         line = run_reference(args, w, rank, world)
         if line is not None:
@@ -392,8 +495,12 @@ def main():
     stages = {}
     for i, nm in enumerate(names):
         stages[nm] = {"ms": float(st[i])}
+    sbytes = score_input_bytes(w)
     stages["score"].update({"tflops": flops / (st[0] * 1e-3) / 1e12,
-                            "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"]})
+                            "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
+                            "frac_of_bf16_peak_one_pass_equiv": flops / 2 / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
+                            "input_gbs": sbytes / (st[0] * 1e-3) / 1e9,
+                            "frac_of_hbm": sbytes / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"]})
     for nm in ("compact", "scatter_back"):
         i = names.index(nm)
         gbs = (bytes_rows + kept * 4) / (st[i] * 1e-3) / 1e9
