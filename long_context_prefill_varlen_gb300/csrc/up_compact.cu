@@ -4,13 +4,16 @@
 // and the drop-history record (section 3.5, "vLLM scheduler integration"), and the end-of-block
 // carry-forward of Eq. 8 (section 3.4).
 //
-// Compaction is four launches, none of which waits on another CTA:
-//   count   per 1024-token tile, the number of kept tokens (16-byte loads of the byte mask)
+// Compaction is three launches (two for streams of at most kScanCountTiles tiles), none of which
+// waits on another CTA:
+//   count   per 1024-token tile, the number of kept tokens (16-byte loads of the byte mask); for
+//           short streams the scan kernel counts the tiles itself
 //   scan    one CTA: tile offsets, and per request prefix(cu[r]) = kept tokens before cu[r]
 //           -> new_cu_seqlens, new_seq_lens, num_actual_tokens, kept_len[layer], drop_layer[layer]
-//   index   per tile: block scan of the flags -> kept_index, out_positions, out_slots
-//   rows    row gather out_hidden[k] = hidden[kept_index[k]] with 16-byte vector copies, one warp
-//           per row, several loads in flight per lane (HBM bound: 2 * T' * hdim * 2 bytes)
+//   gather  persistent CTAs over (tile, part) items, parts chosen so that there are several items per
+//           resident CTA: a scan of the tile's flags gives each kept token its place; part 0 writes
+//           kept_index, out_positions and out_slots, every part copies its share of the kept hidden
+//           rows with 16-byte vectors, one warp per row (HBM bound: 2 * T' * hdim * 2 bytes)
 // Scatter-back is the row copy in the other direction: residual[kept_index[k]] = new_states[k].
 #include <stdint.h>
 
@@ -26,6 +29,9 @@ constexpr int kTile = 1024;          // tokens per tile
 constexpr int kTileThreads = 64;     // 16 flags per thread
 constexpr int kRowThreads = 512;
 constexpr int kRowUnroll = 4;
+constexpr int kGatherThreads = 256;
+constexpr int kMaxParts = 64;          // work items sharing one tile's row copies
+constexpr int kScanCountTiles = 64;    // up to this many tiles the scan kernel counts them itself
 
 struct Layout {
     size_t tile_cnt, tile_off, total;
@@ -92,10 +98,10 @@ __global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __re
 }
 
 __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu,
-                                                    int R, int T, const int* tile_cnt, int* tile_off,
+                                                    int R, int T, int* tile_cnt, int* tile_off,
                                                     int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
                                                     int32_t* kept_len, uint8_t* drop_layer, int layer,
-                                                    int32_t* status) {
+                                                    int32_t* status, int count_here) {
     __shared__ int sh[32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -113,8 +119,22 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
         }
         return;
     }
-    // exclusive scan of the tile counts (tiles split in contiguous chunks over the threads)
     const int tiles = (T + kTile - 1) / kTile;
+    if (count_here) {
+        // a short stream (tiles <= kScanCountTiles): one warp per tile, 16 flags per lane and load
+        for (int i = w; i < tiles; i += blockDim.x / 32) {
+            int c = 0;
+            for (int j = lane; j < kTile / 16; j += 32) {
+                const int64_t t = (int64_t)i * kTile + j * 16;
+                if (t < T) c += count_nonzero_bytes(load_flags16(keep, t, T));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0) tile_cnt[i] = c;
+        }
+        __syncthreads();
+    }
+    // exclusive scan of the tile counts (tiles split in contiguous chunks over the threads)
     const int per = (tiles + blockDim.x - 1) / blockDim.x;
     const int a0 = min(tiles, tid * per), a1 = min(tiles, a0 + per);
     int local = 0;
@@ -166,36 +186,77 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
     }
 }
 
-__global__ void __launch_bounds__(kTileThreads) index_kernel(const uint8_t* __restrict__ keep, int T,
-                                                             const int* __restrict__ tile_off,
-                                                             const int64_t* __restrict__ pos,
-                                                             const int64_t* __restrict__ slots, int32_t* kept_index,
-                                                             int64_t* out_pos, int64_t* out_slots) {
-    __shared__ int sh[16];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
-    const uint4 f = t0 < T ? load_flags16(keep, t0, T) : make_uint4(0, 0, 0, 0);
-    const int c = count_nonzero_bytes(f);
-    int x = c;
+// One warp copies one row of V 16-byte vectors, kRowUnroll loads in flight per lane.
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ s, uint4* __restrict__ d, int V, int lane) {
+    int j = lane;
+    for (; j + 32 * (kRowUnroll - 1) < V; j += 32 * kRowUnroll) {
+        uint4 r[kRowUnroll];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+        for (int u = 0; u < kRowUnroll; ++u) r[u] = __ldcs(s + j + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kRowUnroll; ++u) d[j + 32 * u] = r[u];
     }
-    if (lane == 31) sh[w] = x;
-    __syncthreads();
-    int base = tile_off[blockIdx.x];
-    for (int i = 0; i < w; ++i) base += sh[i];
-    int d = base + x - c;
-    const uint32_t fw[4] = {f.x, f.y, f.z, f.w};
+    for (; j < V; j += 32) d[j] = __ldcs(s + j);
+}
+
+// Items (tile, part) = (item / parts, item % parts), visited round-robin by the persistent CTAs: the
+// tile's kept tokens in ascending order (a scan of its 1024 flags, recomputed by every part), the
+// index/positions/slots rows written by part 0, and the part's contiguous share of the kept hidden rows
+// copied.
+template <bool ROWS>
+__global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* __restrict__ keep, int T, int tiles,
+                                                              int parts, const int* __restrict__ tile_off,
+                                                              const int64_t* __restrict__ pos,
+                                                              const int64_t* __restrict__ slots, int32_t* kept_index,
+                                                              int64_t* out_pos, int64_t* out_slots,
+                                                              const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                                              int V) {
+    __shared__ int s_src[kTile];           // source token of the tile's k-th kept token
+    __shared__ int s_wsum[kTileThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    const int64_t items = (int64_t)tiles * parts;
+    for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
+        const int tile = static_cast<int>(item / parts), part = static_cast<int>(item % parts);
+        const int64_t t0 = (int64_t)tile * kTile + tid * 16;         // threads 0..63 own 16 flags each
+        uint4 f = make_uint4(0, 0, 0, 0);
+        if (tid < kTileThreads && t0 < T) f = load_flags16(keep, t0, T);
+        const int c = count_nonzero_bytes(f);
+        int x = c;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        if ((fw[i >> 2] >> (8 * (i & 3))) & 0xFFu) {
-            const int64_t src = t0 + i;
-            kept_index[d] = static_cast<int32_t>(src);
-            if (out_pos) out_pos[d] = pos[src];
-            if (out_slots) out_slots[d] = slots[src];
-            ++d;
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        __syncthreads();                    // the previous item is done with s_src and s_wsum
+        if (lane == 31 && w < kTileThreads / 32) s_wsum[w] = x;
+        __syncthreads();
+        if (tid < kTileThreads) {
+            int d = x - c;
+            for (int i = 0; i < w; ++i) d += s_wsum[i];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t wv = i < 4 ? f.x : i < 8 ? f.y : i < 12 ? f.z : f.w;
+                if ((wv >> (8 * (i & 3))) & 0xFFu) s_src[d++] = static_cast<int>(t0 + i);
+            }
+        }
+        int cnt = 0;
+#pragma unroll
+        for (int i = 0; i < kTileThreads / 32; ++i) cnt += s_wsum[i];
+        __syncthreads();
+        const int base = tile_off[tile];
+        if (part == 0) {
+            for (int k = tid; k < cnt; k += kGatherThreads) {
+                const int sidx = s_src[k];
+                kept_index[base + k] = sidx;
+                if (out_pos) out_pos[base + k] = pos[sidx];
+                if (out_slots) out_slots[base + k] = slots[sidx];
+            }
+        }
+        if (ROWS) {
+            const int per = (cnt + parts - 1) / parts;
+            const int k0 = part * per, k1 = min(cnt, k0 + per);
+            for (int k = k0 + w; k < k1; k += kGatherThreads / 32)
+                copy_row(src + (int64_t)s_src[k] * V, dst + (int64_t)(base + k) * V, V, lane);
         }
     }
 }
@@ -215,18 +276,65 @@ __global__ void __launch_bounds__(kRowThreads) rows_kernel(const uint4* __restri
     const int warps = gridDim.x * (kRowThreads / 32);
     for (int k = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); k < n; k += warps) {
         const int64_t other = idx[k];
-        const uint4* s = src + (GATHER ? other : (int64_t)k) * V;
-        uint4* d = dst + (GATHER ? (int64_t)k : other) * V;
-        int j = lane;
-        for (; j + 32 * (kRowUnroll - 1) < V; j += 32 * kRowUnroll) {
-            uint4 r[kRowUnroll];
-#pragma unroll
-            for (int u = 0; u < kRowUnroll; ++u) r[u] = __ldcs(s + j + 32 * u);
-#pragma unroll
-            for (int u = 0; u < kRowUnroll; ++u) d[j + 32 * u] = r[u];
-        }
-        for (; j < V; j += 32) d[j] = __ldcs(s + j);
+        copy_row(src + (GATHER ? other : (int64_t)k) * V, dst + (GATHER ? (int64_t)k : other) * V, V, lane);
     }
+}
+
+// CTAs of a kernel that are resident on the whole GPU at once (occupancy x SMs), once per process: a
+// persistent grid of exactly this size runs in one wave.
+template <typename K>
+static int resident_ctas(K kernel, int threads) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, 0) != cudaSuccess || per_sm <= 0)
+        per_sm = 1;
+    return per_sm * num_sms();
+}
+static int scatter_resident() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] { n = resident_ctas(rows_kernel<false>, kRowThreads); });
+    return n;
+}
+
+// CTAs of gather_kernel that are resident on the whole GPU at once (occupancy x SMs), once per process.
+template <bool ROWS>
+static int gather_resident() {
+    static int n = 0;
+    static std::once_flag once;
+    std::call_once(once, [] { n = resident_ctas(gather_kernel<ROWS>, kGatherThreads); });
+    return n;
+}
+
+// The launches of one compaction, on the caller's workspace or the fixed scratch alike.
+static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int Ti, const uint16_t* hidden,
+                              int hdim, const int64_t* positions, const int64_t* slots, uint16_t* out_hidden,
+                              int64_t* out_positions, int64_t* out_slots, int32_t* kept_index, int32_t* new_cu,
+                              int32_t* new_len, int32_t* num_actual, int32_t* kept_len, uint8_t* drop_layer,
+                              int layer, int* tile_cnt, int* tile_off, int32_t* status, cudaStream_t st) {
+    const int tiles = static_cast<int>(cdiv(Ti, kTile));
+    const int count_here = tiles <= kScanCountTiles ? 1 : 0;
+    if (tiles > 0 && !count_here) {
+        count_kernel<<<tiles, kTileThreads, 0, st>>>(keep, Ti, tile_cnt);
+        count_launch();
+    }
+    scan_kernel<<<1, 1024, 0, st>>>(keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len,
+                                    drop_layer, layer, status, count_here);
+    count_launch();
+    if (tiles == 0) return;
+    // persistent CTAs: as many as fit on the GPU at once; parts per tile so that every resident CTA
+    // has several items (fine-grained enough that the last round is short)
+    const int resident = hidden ? gather_resident<true>() : gather_resident<false>();
+    const int parts = hidden ? static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxParts, cdiv(4 * resident, tiles))))
+                             : 1;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((int64_t)tiles * parts, resident)));
+    if (hidden)
+        gather_kernel<true><<<grid, kGatherThreads, 0, st>>>(
+            keep, Ti, tiles, parts, tile_off, positions, slots, kept_index, out_positions, out_slots,
+            reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), hdim / 8);
+    else
+        gather_kernel<false><<<grid, kGatherThreads, 0, st>>>(keep, Ti, tiles, 1, tile_off, positions, slots,
+                                                            kept_index, out_positions, out_slots, nullptr, nullptr, 0);
+    count_launch();
 }
 
 }  // namespace compact
@@ -260,29 +368,9 @@ extern "C" up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seq
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     int* tile_cnt = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + Lw.tile_cnt);
     int* tile_off = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + Lw.tile_off);
-    const int tiles = static_cast<int>(cdiv(T, compact::kTile));
-    const int Ti = static_cast<int>(T);
-    if (tiles > 0) {
-        compact::count_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_cnt);
-        count_launch();
-    }
-    compact::scan_kernel<<<1, 1024, 0, st>>>(token_keep, cu_seqlens, R, Ti, tile_cnt, tile_off, new_cu_seqlens,
-                                             new_seq_lens, num_actual_tokens, kept_len, drop_layer, layer,
-                                             dev_status);
-    count_launch();
-    if (tiles > 0) {
-        compact::index_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_off, positions, slots,
-                                                                      kept_index, out_positions, out_slots);
-        count_launch();
-        if (hidden) {
-            const int V = hdim / 8;
-            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T, compact::kRowThreads / 32), 4 * num_sms()));
-            compact::rows_kernel<true><<<grid, compact::kRowThreads, 0, st>>>(
-                reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), kept_index,
-                num_actual_tokens, T, V, dev_status);
-            count_launch();
-        }
-    }
+    compact::launch_compaction(token_keep, cu_seqlens, R, static_cast<int>(T), hidden, hdim, positions, slots,
+                               out_hidden, out_positions, out_slots, kept_index, new_cu_seqlens, new_seq_lens,
+                               num_actual_tokens, kept_len, drop_layer, layer, tile_cnt, tile_off, dev_status, st);
     return check_launch();
 }
 
@@ -294,7 +382,9 @@ extern "C" up_status up_scatter_back(const uint16_t* new_states, const int32_t* 
     if (hdim <= 0 || hdim % 8 != 0 || !aligned16(new_states) || !aligned16(residual)) return UP_ERR_SHAPE;
     if (T_upper == 0) return UP_OK;
     const int V = hdim / 8;
-    const int grid = static_cast<int>(std::min<int64_t>(cdiv(T_upper, compact::kRowThreads / 32), 4 * num_sms()));
+    // one wave of persistent CTAs (a grid larger than what is resident leaves a trailing partial wave)
+    const int grid = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(cdiv(T_upper, compact::kRowThreads / 32), compact::scatter_resident())));
     compact::rows_kernel<false><<<grid, compact::kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         reinterpret_cast<const uint4*>(new_states), reinterpret_cast<uint4*>(residual), kept_index, num_actual_tokens,
         T_upper, V, dev_status);
@@ -370,29 +460,9 @@ extern "C" up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t
     if (scratch == nullptr) return err;
     int* tile_cnt = scratch;
     int* tile_off = scratch + compact::kNoAllocMaxTiles + 1;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int tiles = static_cast<int>(cdiv(T, compact::kTile));
-    const int Ti = static_cast<int>(T);
-    if (tiles > 0) {
-        compact::count_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_cnt);
-        count_launch();
-    }
-    compact::scan_kernel<<<1, 1024, 0, st>>>(token_keep, cu_seqlens, R, Ti, tile_cnt, tile_off, new_cu_seqlens,
-                                             new_seq_lens, num_actual_tokens, kept_len, drop_layer, layer,
-                                             dev_status);
-    count_launch();
-    if (tiles > 0) {
-        compact::index_kernel<<<tiles, compact::kTileThreads, 0, st>>>(token_keep, Ti, tile_off, positions, slots,
-                                                                      kept_index, out_positions, out_slots);
-        count_launch();
-        if (hidden) {
-            const int V = hdim / 8;
-            const int grid = static_cast<int>(std::min<int64_t>(cdiv(T, compact::kRowThreads / 32), 4 * num_sms()));
-            compact::rows_kernel<true><<<grid, compact::kRowThreads, 0, st>>>(
-                reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), kept_index,
-                num_actual_tokens, T, V, dev_status);
-            count_launch();
-        }
-    }
+    compact::launch_compaction(token_keep, cu_seqlens, R, static_cast<int>(T), hidden, hdim, positions, slots,
+                               out_hidden, out_positions, out_slots, kept_index, new_cu_seqlens, new_seq_lens,
+                               num_actual_tokens, kept_len, drop_layer, layer, tile_cnt, tile_off, dev_status,
+                               static_cast<cudaStream_t>(stream));
     return check_launch();
 }
