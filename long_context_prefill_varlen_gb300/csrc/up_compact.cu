@@ -90,6 +90,8 @@ __device__ __forceinline__ int block_reduce(int v, int* sh) {
 }
 
 __global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __restrict__ keep, int T, int* tile_cnt) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int sh[9];
     const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
     const int c = t0 < T ? count_nonzero_bytes(load_flags16(keep, t0, T)) : 0;
@@ -102,6 +104,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
                                                     int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
                                                     int32_t* kept_len, uint8_t* drop_layer, int layer,
                                                     int32_t* status, int count_here) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int sh[32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -211,6 +215,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* _
                                                               int64_t* out_pos, int64_t* out_slots,
                                                               const uint4* __restrict__ src, uint4* __restrict__ dst,
                                                               int V) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_src[kTile];           // source token of the tile's k-th kept token
     __shared__ int s_wsum[kTileThreads / 32];
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -267,6 +273,8 @@ __global__ void __launch_bounds__(kRowThreads) rows_kernel(const uint4* __restri
                                                            const int32_t* __restrict__ idx,
                                                            const int32_t* __restrict__ count, int64_t T_upper,
                                                            int V, int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     const int n = *count;
     if (n < 0 || n > T_upper) {
         if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, UP_DEV_BAD_TOKEN_COUNT);
@@ -314,11 +322,12 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
     const int tiles = static_cast<int>(cdiv(Ti, kTile));
     const int count_here = tiles <= kScanCountTiles ? 1 : 0;
     if (tiles > 0 && !count_here) {
-        count_kernel<<<tiles, kTileThreads, 0, st>>>(keep, Ti, tile_cnt);
+        launch_pdl(count_kernel, dim3(tiles), dim3(kTileThreads), 0, st, keep, Ti, tile_cnt);
         count_launch();
     }
-    scan_kernel<<<1, 1024, 0, st>>>(keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len,
-                                    drop_layer, layer, status, count_here);
+    launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st,
+        keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len, drop_layer, layer, status,
+        count_here);
     count_launch();
     if (tiles == 0) return;
     // persistent CTAs: as many as fit on the GPU at once; parts per tile so that every resident CTA
@@ -328,12 +337,13 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
                              : 1;
     const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((int64_t)tiles * parts, resident)));
     if (hidden)
-        gather_kernel<true><<<grid, kGatherThreads, 0, st>>>(
+        launch_pdl(gather_kernel<true>, dim3(grid), dim3(kGatherThreads), 0, st, 
             keep, Ti, tiles, parts, tile_off, positions, slots, kept_index, out_positions, out_slots,
             reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), hdim / 8);
     else
-        gather_kernel<false><<<grid, kGatherThreads, 0, st>>>(keep, Ti, tiles, 1, tile_off, positions, slots,
-                                                            kept_index, out_positions, out_slots, nullptr, nullptr, 0);
+        launch_pdl(gather_kernel<false>, dim3(grid), dim3(kGatherThreads), 0, st,
+            keep, Ti, tiles, 1, tile_off, positions, slots, kept_index, out_positions, out_slots, nullptr,
+            nullptr, 0);
     count_launch();
 }
 
@@ -385,9 +395,9 @@ extern "C" up_status up_scatter_back(const uint16_t* new_states, const int32_t* 
     // one wave of persistent CTAs (a grid larger than what is resident leaves a trailing partial wave)
     const int grid = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>(cdiv(T_upper, compact::kRowThreads / 32), compact::scatter_resident())));
-    compact::rows_kernel<false><<<grid, compact::kRowThreads, 0, static_cast<cudaStream_t>(stream)>>>(
-        reinterpret_cast<const uint4*>(new_states), reinterpret_cast<uint4*>(residual), kept_index, num_actual_tokens,
-        T_upper, V, dev_status);
+    launch_pdl(compact::rows_kernel<false>, dim3(grid), dim3(compact::kRowThreads), 0, static_cast<cudaStream_t>(stream),
+        reinterpret_cast<const uint4*>(new_states), reinterpret_cast<uint4*>(residual), kept_index,
+        num_actual_tokens, T_upper, V, dev_status);
     count_launch();
     return check_launch();
 }

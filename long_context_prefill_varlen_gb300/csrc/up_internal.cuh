@@ -20,12 +20,36 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Every kernel of the library is launched with programmatic dependent launch: its CTAs may become
+// resident (and set up shared memory, barriers and TMEM) while the previous kernel in the stream is
+// still finishing.  Each kernel calls pdl_wait() before its first access to global memory, which
+// returns once the previous grid has completed and its writes are visible, and then pdl_trigger(), so
+// that at most two grids of the stream overlap.  Outside such a launch both are no-ops.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ------------------------------------------------------------------------------------------------
 // device side: status word
 
 __device__ __forceinline__ void set_status(int32_t* st, int code) {
     if (st) atomicCAS(st, 0, code);
 }
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -35,6 +35,8 @@ namespace meta {
 __global__ void slot_kernel(const int64_t* __restrict__ pos, const int32_t* __restrict__ cu, int R, int64_t T_upper,
                             const int32_t* __restrict__ num_tokens, const int32_t* __restrict__ table, int max_blocks,
                             int B, int64_t* slots, int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     int64_t n = T_upper;
     if (num_tokens) {
         const int c = *num_tokens;
@@ -64,6 +66,8 @@ __global__ void slot_kernel(const int64_t* __restrict__ pos, const int32_t* __re
 __global__ void seqused_kernel(const int32_t* __restrict__ kept_len, const uint8_t* __restrict__ drop_layer, int L,
                                int R, int layer, const int32_t* __restrict__ orig_len,
                                const int32_t* __restrict__ kv_len, int32_t* seqused) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_prev;
     if (threadIdx.x == 0) {
         int prev = -1;
@@ -91,9 +95,8 @@ extern "C" up_status up_slot_mapping(const int64_t* positions, const int32_t* cu
     if (R <= 0 || T_upper < 0 || max_blocks <= 0 || B <= 0) return UP_ERR_ARG;
     if (T_upper == 0) return UP_OK;
     const int grid = static_cast<int>(std::min<int64_t>(cdiv(T_upper, 256), 8 * num_sms()));
-    meta::slot_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(positions, cu_seqlens, R, T_upper,
-                                                                            num_tokens, block_table, max_blocks, B,
-                                                                            slots, dev_status);
+    launch_pdl(meta::slot_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
+        positions, cu_seqlens, R, T_upper, num_tokens, block_table, max_blocks, B, slots, dev_status);
     count_launch();
     return check_launch();
 }
@@ -103,8 +106,8 @@ extern "C" up_status up_seqused(const int32_t* kept_len, const uint8_t* drop_lay
     if (!kept_len || !drop_layer || !orig_len || !kv_len || !seqused) return UP_ERR_ARG;
     if (L <= 0 || R <= 0 || layer < 0 || layer >= L) return UP_ERR_ARG;
     const int grid = static_cast<int>(std::min<int64_t>(cdiv(R, 256), 4 * num_sms()));
-    meta::seqused_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(kept_len, drop_layer, L, R, layer,
-                                                                               orig_len, kv_len, seqused);
+    launch_pdl(meta::seqused_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
+        kept_len, drop_layer, L, R, layer, orig_len, kv_len, seqused);
     count_launch();
     return check_launch();
 }

@@ -144,6 +144,8 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sh, int* to
 }
 
 __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int s_bad;
     __shared__ int s_scan[32];
     const int tid = threadIdx.x;
@@ -819,6 +821,8 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
 // Fold each query row's pass-1 partials (one per work item of its unit, in item order) into
 // c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
 __global__ void __launch_bounds__(256) merge_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
     if (__ldcg(P.n_items + 1) == 0) return;
     const int lane = threadIdx.x & 31;
     const int64_t rows_all = (int64_t)P.R * P.units_per_req * P.slab_rows;
@@ -896,6 +900,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = static_cast<uint32_t>(uni(static_cast<int>(*S.tmem_holder)));
 
+    // the set-up above touched only this CTA's shared memory and TMEM; global data from here on
+    pdl_wait();
+    pdl_trigger();
     const int n_items = uni(__ldcg(P.n_items));
     const int it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
     const int it1 = static_cast<int>((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
@@ -950,6 +957,8 @@ __device__ __forceinline__ float sum_parts(const float* x, int64_t stride, int p
 }
 
 __global__ void finalize_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
     if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
     const int parts = P.units_per_req * 4;       // (unit, warpgroup) partials, summed in a fixed order
     const int nb_total = P.cb[P.R];
@@ -1012,9 +1021,9 @@ static cudaError_t launch_pass(const CUtensorMap& q, const CUtensorMap& k, const
                                     kSmemBytes);
     });
     if (attr != cudaSuccess) return attr;
-    score_pass_kernel<PASS, NC><<<grid, kThreads, kSmemBytes, st>>>(q, k, P);
+    const cudaError_t e = launch_pdl(score_pass_kernel<PASS, NC>, dim3(grid), dim3(kThreads), kSmemBytes, st, q, k, P);
     count_launch();
-    return cudaGetLastError();
+    return e;
 }
 
 template <int NC>
@@ -1023,9 +1032,9 @@ static cudaError_t launch_both(const CUtensorMap& q, const CUtensorMap& k, const
     cudaError_t e = launch_pass<1, NC>(q, k, P, grid, st);
     if (e != cudaSuccess) return e;
     const int mgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(merge_rows, 8), 16 * num_sms())));
-    merge_kernel<<<mgrid, 256, 0, st>>>(P);
+    e = launch_pdl(merge_kernel, dim3(mgrid), dim3(256), 0, st, P);
     count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (e != cudaSuccess) return e;
     return launch_pass<2, NC>(q, k, P, grid, st);
 }
 
@@ -1095,9 +1104,9 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.token_scores = token_scores;
     P.status = dev_status;
 
-    plan_kernel<<<1, 1024, 0, st>>>(P);
+    cudaError_t le = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, P);
     count_launch();
-    if (cudaGetLastError() != cudaSuccess) return UP_ERR_CUDA;
+    if (le != cudaSuccess) return UP_ERR_CUDA;
     if (T > 0) {
         CUtensorMap tq, tk;
         if (!make_map(&tq, Q, T, Hq, dk, g.box_rows) || !make_map(&tk, K, T, Hkv, dk, kTileKeys)) return UP_ERR_CUDA;
@@ -1112,7 +1121,7 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
         if (e != cudaSuccess) return UP_ERR_CUDA;
     }
     const int fgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(4 * num_sms(), cdiv(std::max<int64_t>(nb_cap, T), 256))));
-    finalize_kernel<<<fgrid, 256, 0, st>>>(P);
+    le = launch_pdl(finalize_kernel, dim3(fgrid), dim3(256), 0, st, P);
     count_launch();
-    return cudaGetLastError() == cudaSuccess ? UP_OK : UP_ERR_CUDA;
+    return le == cudaSuccess ? UP_OK : UP_ERR_CUDA;
 }

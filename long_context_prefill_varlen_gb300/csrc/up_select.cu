@@ -67,6 +67,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
                                                           const int32_t* __restrict__ cu, int R, int T, int64_t nb_cap,
                                                           int G, int n, int A, double p, uint8_t* block_keep,
                                                           uint8_t* token_keep, int32_t* kstar, int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     extern __shared__ __align__(16) uint8_t sm[];
     uint64_t* keys = reinterpret_cast<uint64_t*>(sm);                              // [8192]
     uint64_t* alt = keys + UP_MAX_BLOCKS_PER_REQUEST;                              // [8192]
@@ -233,6 +235,8 @@ constexpr int kSmemBytes = 2 * UP_MAX_BLOCKS_PER_REQUEST * 8 + kRadix * kWarps *
 
 __global__ void __launch_bounds__(1024) cu_blocks_kernel(const int32_t* cu, int R, int T, int G, int32_t* cb,
                                                          int32_t* status) {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int sh[32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
@@ -286,8 +290,8 @@ extern "C" up_status up_make_cu_blocks(const int32_t* cu_seqlens, int R, int64_t
                                        int32_t* dev_status, void* stream) {
     if (!cu_seqlens || !cu_blocks || !dev_status) return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || G <= 0) return UP_ERR_ARG;
-    select::cu_blocks_kernel<<<1, 1024, 0, static_cast<cudaStream_t>(stream)>>>(cu_seqlens, R, static_cast<int>(T),
-                                                                                G, cu_blocks, dev_status);
+    launch_pdl(select::cu_blocks_kernel, dim3(1), dim3(1024), 0, static_cast<cudaStream_t>(stream),
+        cu_seqlens, R, static_cast<int>(T), G, cu_blocks, dev_status);
     count_launch();
     return check_launch();
 }
@@ -310,8 +314,8 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
             return UP_ERR_CUDA;
         attr_done[dev] = 1;
     }
-    select::select_kernel<<<R, select::kThreads, select::kSmemBytes, static_cast<cudaStream_t>(stream)>>>(
-        block_scores, cu_blocks, cu_seqlens, R, static_cast<int>(T), nb_cap, G, n, A, p, block_keep, token_keep,
+    launch_pdl(select::select_kernel, dim3(R), dim3(select::kThreads), select::kSmemBytes,
+        static_cast<cudaStream_t>(stream), block_scores, cu_blocks, cu_seqlens, R, static_cast<int>(T), nb_cap, G, n, A, p, block_keep, token_keep,
         kstar, dev_status);
     count_launch();
     return check_launch();
