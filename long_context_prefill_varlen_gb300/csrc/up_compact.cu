@@ -28,7 +28,7 @@ namespace compact {
 constexpr int kTile = 1024;          // tokens per tile
 constexpr int kTileThreads = 64;     // 16 flags per thread
 constexpr int kRowThreads = 512;
-constexpr int kRowUnroll = 4;
+constexpr int kRowUnroll = 8;
 constexpr int kGatherThreads = 256;
 constexpr int kMaxParts = 64;          // work items sharing one tile's row copies
 constexpr int kScanCountTiles = 64;    // up to this many tiles the scan kernel counts them itself
