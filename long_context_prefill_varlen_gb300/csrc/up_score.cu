@@ -591,6 +591,24 @@ __device__ __forceinline__ void key_chunk_full(const uint32_t (&v)[16], const fl
     }
 }
 
+// pass 2 for slices of eight chunks (one whole job per warpgroup): the chunk's normalisers come from
+// the lanes that hold them by warp shuffle instead of broadcast shared-memory loads, which compete with
+// the MMA's shared-memory operand reads.  Lane L holds -c of column 32 * r + L of the slice in cr
+// (r = chunk / 2); the chunk's column 16 * half + i of that 32-column group comes from lane 16 * half + i.
+__device__ __forceinline__ void key_chunk_full_sh(const uint32_t (&v)[16], float cr, int half, float a,
+                                                  uint64_t (&acc)[2]) {
+    const uint64_t a2 = pk2(a, a);
+#pragma unroll
+    for (int c = 0; c < 16; c += 4) {
+        const float n0 = __shfl_sync(0xffffffffu, cr, half * 16 + c);
+        const float n1 = __shfl_sync(0xffffffffu, cr, half * 16 + c + 1);
+        const float n2 = __shfl_sync(0xffffffffu, cr, half * 16 + c + 2);
+        const float n3 = __shfl_sync(0xffffffffu, cr, half * 16 + c + 3);
+        acc[0] = add2(acc[0], p2(v, c, a2, pk2(n0, n1)));
+        acc[1] = add2(acc[1], p2(v, c + 2, a2, pk2(n2, n3)));
+    }
+}
+
 // pass 2 with the causal mask: key i is visible to the query row at local position pos iff i <= pos.
 // The slab's rows are head-major (row qg is window position qg % n of head qg / n) and qg0 and n are
 // multiples of 16, so the chunk's 16 rows are window positions t0 .. t0 + 15 of one head: one modulo
@@ -625,18 +643,26 @@ __device__ __forceinline__ void release_tmem(const Smem& S, uint32_t buf, int la
 template <int PASS, int NCH>
 __device__ __forceinline__ void run_job_fast(const Smem& S, uint32_t ta, uint32_t buf, int lane, float a,
                                              const float* ncv0, float& m, float& l, uint64_t (&acc)[2]) {
+    constexpr bool kShfl = PASS == 2 && NCH == 8;
     uint32_t va[16], vb[16];
+    float creg[NCH / 2];
+    if (kShfl) {
+#pragma unroll
+        for (int r = 0; r < NCH / 2; ++r) creg[r] = ncv0[32 * r + lane];
+    }
     tmem_ld16(ta, va);
     tmem_wait_pin(va);
 #pragma unroll
     for (int ch = 0; ch < NCH; ch += 2) {
         tmem_ld16(ta + (ch + 1) * 16, vb);
         if (PASS == 1) row_chunk_full(va, a, m, l);
+        else if (kShfl) key_chunk_full_sh(va, creg[ch / 2], 0, a, acc);
         else key_chunk_full(va, ncv0 + ch * 16, a, acc);
         tmem_wait_pin(vb);
         if (ch + 2 < NCH) tmem_ld16(ta + (ch + 2) * 16, va);
         else release_tmem(S, buf, lane);
         if (PASS == 1) row_chunk_full(vb, a, m, l);
+        else if (kShfl) key_chunk_full_sh(vb, creg[ch / 2], 1, a, acc);
         else key_chunk_full(vb, ncv0 + (ch + 1) * 16, a, acc);
         if (ch + 2 < NCH) tmem_wait_pin(va);
     }
@@ -941,18 +967,18 @@ __device__ __forceinline__ int find_segment(const int32_t* cuts, int R, int x) {
     return lo;
 }
 
-// sum of parts values x[k * stride], k = 0, 1, ... in that order; the loads go out eight at a time
+// sum of parts values x[k * stride], k = 0, 1, ... in that order; the loads go out 32 at a time (the
+// usual count of partials: one latency round), entries past the end add +0 and change nothing
 __device__ __forceinline__ float sum_parts(const float* x, int64_t stride, int parts) {
+    constexpr int kBatch = 32;
     float s = 0.f;
-    int k = 0;
-    for (; k + 8 <= parts; k += 8) {
-        float v[8];
+    for (int k = 0; k < parts; k += kBatch) {
+        float v[kBatch];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = __ldcg(x + (size_t)(k + i) * stride);
+        for (int i = 0; i < kBatch; ++i) v[i] = k + i < parts ? __ldcg(x + (size_t)(k + i) * stride) : 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) s += v[i];
+        for (int i = 0; i < kBatch; ++i) s += v[i];
     }
-    for (; k < parts; ++k) s += __ldcg(x + (size_t)k * stride);
     return s;
 }
 
