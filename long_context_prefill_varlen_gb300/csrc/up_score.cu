@@ -697,6 +697,7 @@ __device__ __forceinline__ void run_job_slow(const Smem& S, uint32_t ta, uint32_
 
 template <int PASS, int NCH>
 __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
+    if (PASS == 2) pdl_wait();                  // the normalisers (merge kernel) are read below
     volatile int* abort_flag = S.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int et = threadIdx.x - 64;            // 0..511
@@ -926,8 +927,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = static_cast<uint32_t>(uni(static_cast<int>(*S.tmem_holder)));
 
-    // the set-up above touched only this CTA's shared memory and TMEM; global data from here on
-    pdl_wait();
+    // The set-up above touched only this CTA's shared memory and TMEM.  Pass 1 reads the work items its
+    // predecessor (the plan kernel) writes, so every warp waits here.  Pass 2's producer and MMA warps
+    // read only Q, K and the items, complete since before pass 1 ran, so they start at once; only its
+    // epilogue waits, for the row normalisers of its predecessor (the merge kernel).
+    if (PASS == 1) pdl_wait();
     pdl_trigger();
     const int n_items = uni(__ldcg(P.n_items));
     const int it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
