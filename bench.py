@@ -207,6 +207,8 @@ def run_gb300(args, w, rank, world):
     step.check()
     step_ms = np.array([a.elapsed_time(b) for a, b in ev])
     ms = float(step_ms.mean())
+    spread = {"median": float(np.median(step_ms)), "p10": float(np.percentile(step_ms, 10)),
+              "p90": float(np.percentile(step_ms, 90)), "max": float(step_ms.max())}
     if world > 1:
         t = torch.tensor([ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -227,7 +229,7 @@ def run_gb300(args, w, rank, world):
     for k in range(nb):
         for i in range(nst - 1):
             stage_ms[k, i] = marks[k][i].elapsed_time(marks[k][i + 1])
-    return dict(ms=ms, eager_ms=float(stage_ms.sum(axis=1).mean()), stage_ms=stage_ms.mean(axis=0),
+    return dict(ms=ms, spread=spread, eager_ms=float(stage_ms.sum(axis=1).mean()), stage_ms=stage_ms.mean(axis=0),
                 launches=launches, clocks=clocks, kept=kept,
                 kstar=step.kstar.cpu().tolist(), step=step, inputs=inputs, run_step=run_step, dev=dev,
                 flush=flush, geometry=dict(L=L, layer=layer, B=B, table=table, orig_len=orig_len, kv_len=kv_len))
@@ -565,7 +567,8 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
             "roofline": rl, "gpu_launches": int(res["launches"]), "clocks": res["clocks"],
             "score_select_compact_tokens_per_s": T_all / (ssc * 1e-3), "kept_tokens": kept,
-            "kstar": res["kstar"][:8], "eager_ms_per_step": res["eager_ms"], "stages": stages}
+            "kstar": res["kstar"][:8], "ms_per_step_spread": res["spread"], "eager_ms_per_step": res["eager_ms"],
+            "stages": stages}
     if not args.no_e2e:
         line["e2e"] = e2e_measure(args, w, res)
     if world == 1 and not args.no_cpu_baseline:
