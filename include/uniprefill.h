@@ -103,7 +103,8 @@ up_status up_make_cu_blocks(const int32_t* cu_seqlens, int R, int64_t T, int G,
  *   kv(h) = h / (Hq / Hkv).  The softmax normalises over the complete key range before any
  *   block reduction, via two passes (row max/sum, then recompute) [UP 3.5 "Kernel design"];
  *   S is never materialised.
- * Q: bf16 [T, Hq, dk] (only each request's last n rows are read); K: bf16 [T, Hkv, dk].
+ * Q: bf16 [T, Hq, dk] (only each request's last n rows are read); K: bf16 [T, Hkv, dk]; both may
+ * be NULL when T = 0.
  * Both 16-byte aligned.  dk in {64, 128, 256}; Hq % Hkv == 0; G in {16, 32, 64, 128};
  * n in {16, 32, 64, 128} or a multiple of 128 up to 1024.  sm_scale is usually 1/sqrt(dk).
  * block_scores: fp32 [nb_cap] (entries cu_blocks[r] .. cu_blocks[r+1]-1 written).
@@ -123,7 +124,8 @@ up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const int32_t* c
  *   token_keep_i = [block(i) among the first k*] or i < A (sinks) or i >= N - n (window);
  *   block_keep_g = any token of B_g kept.
  * block_scores: fp32 [nb_cap], finite and >= 0.  p in (0, 1]; A >= 0; n >= 1; G a power of two.
- * block_keep: u8 [nb_cap]; token_keep: u8 [T]; kstar: int32 [R] (0 for empty requests).
+ * block_keep: u8 [nb_cap]; token_keep: u8 [T] (may be NULL when T = 0); kstar: int32 [R] (0 for
+ * empty requests).
  * At most UP_MAX_BLOCKS_PER_REQUEST blocks per request (else UP_DEV_TOO_MANY_BLOCKS). */
 up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,
                          const int32_t* cu_seqlens, int R, int64_t T, int64_t nb_cap,
@@ -142,7 +144,8 @@ up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,
  *   num_actual_tokens = T', int32 [1] (stays on the device; buffers are sized by T)
  *   kept_len[layer*R + r] = new_seq_lens[r] and drop_layer[layer] = 1 record the drop history
  *   {(l_k, s_k^r)} of [UP 3.5] (both optional; kept_len int32 [L, R], drop_layer u8 [L]).
- * hdim % 8 == 0; hidden/out_hidden 16-byte aligned; token_keep 16-byte aligned.
+ * hdim % 8 == 0; hidden/out_hidden 16-byte aligned; token_keep 16-byte aligned (may be NULL when
+ * T = 0, as may hidden/positions/slots and their outputs).
  * ws: up_compact_workspace_bytes(R, T) bytes. */
 up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seqlens, int R, int64_t T,
                      const uint16_t* hidden, int hdim, const int64_t* positions, const int64_t* slots,
@@ -176,7 +179,8 @@ up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t* cu_seqlen
 /* End-of-block carry-forward [UP 3.4, Eq. 8], in place:
  *   residual[kept_index[k], :] = new_states[k, :]  for k < *num_actual_tokens;
  *   rows of dropped tokens are not touched (they keep H^(b,0)).
- * new_states: bf16 [T_upper, hdim]; residual: bf16 [T_upper, hdim]; both 16-byte aligned;
+ * new_states: bf16 [T_upper, hdim]; residual: bf16 [T_upper, hdim]; both 16-byte aligned (with
+ * T_upper = 0 nothing is read or written and every pointer may be NULL);
  * hdim % 8 == 0.  kept_index/num_actual_tokens as produced by up_compact. */
 up_status up_scatter_back(const uint16_t* new_states, const int32_t* kept_index,
                           const int32_t* num_actual_tokens, int64_t T_upper, int hdim,
@@ -186,7 +190,8 @@ up_status up_scatter_back(const uint16_t* new_states, const int32_t* kept_index,
  *   slot_t = block_table[r_t * max_blocks + floor(p_t / B)] * B + (p_t mod B)
  * r_t = the request of token t under cu_seqlens (e.g. the compacted new_cu_seqlens), p_t =
  * positions[t] (int64).  Tokens t < *num_tokens (or < T_upper if num_tokens is NULL).
- * block_table: int32 [R, max_blocks]; slots: int64 [T_upper].  A position outside
+ * block_table: int32 [R, max_blocks]; slots: int64 [T_upper] (positions and slots may be NULL
+ * when T_upper = 0).  A position outside
  * [0, max_blocks*B) writes -1 and sets UP_DEV_BAD_POSITION. */
 up_status up_slot_mapping(const int64_t* positions, const int32_t* cu_seqlens, int R, int64_t T_upper,
                           const int32_t* num_tokens, const int32_t* block_table, int max_blocks, int B,

@@ -363,8 +363,9 @@ extern "C" up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seq
                                 int32_t* kept_index, int32_t* new_cu_seqlens, int32_t* new_seq_lens,
                                 int32_t* num_actual_tokens, int32_t* kept_len, uint8_t* drop_layer, int L, int layer,
                                 void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
-    if (!token_keep || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens || !num_actual_tokens ||
-        !ws || !dev_status)
+    // token_keep may be NULL for a batch without tokens (T = 0)
+    if ((T > 0 && !token_keep) || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens ||
+        !num_actual_tokens || !ws || !dev_status)
         return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31)) return UP_ERR_ARG;
     if ((hidden == nullptr) != (out_hidden == nullptr) || (positions == nullptr) != (out_positions == nullptr) ||
@@ -387,10 +388,11 @@ extern "C" up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seq
 extern "C" up_status up_scatter_back(const uint16_t* new_states, const int32_t* kept_index,
                                      const int32_t* num_actual_tokens, int64_t T_upper, int hdim, uint16_t* residual,
                                      int32_t* dev_status, void* stream) {
-    if (!new_states || !kept_index || !num_actual_tokens || !residual || !dev_status) return UP_ERR_ARG;
     if (T_upper < 0 || T_upper >= (int64_t(1) << 31)) return UP_ERR_ARG;
-    if (hdim <= 0 || hdim % 8 != 0 || !aligned16(new_states) || !aligned16(residual)) return UP_ERR_SHAPE;
-    if (T_upper == 0) return UP_OK;
+    if (hdim <= 0 || hdim % 8 != 0) return UP_ERR_SHAPE;
+    if (T_upper == 0) return UP_OK;        // no rows: the buffers may be empty (NULL)
+    if (!new_states || !kept_index || !num_actual_tokens || !residual || !dev_status) return UP_ERR_ARG;
+    if (!aligned16(new_states) || !aligned16(residual)) return UP_ERR_SHAPE;
     const int V = hdim / 8;
     // one wave of persistent CTAs (a grid larger than what is resident leaves a trailing partial wave)
     const int grid = static_cast<int>(
@@ -454,8 +456,8 @@ extern "C" up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t
                                         int64_t* out_slots, int32_t* kept_index, int32_t* new_cu_seqlens,
                                         int32_t* new_seq_lens, int32_t* num_actual_tokens, int32_t* kept_len,
                                         uint8_t* drop_layer, int L, int layer, int32_t* dev_status, void* stream) {
-    if (!token_keep || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens || !num_actual_tokens ||
-        !dev_status)
+    if ((T > 0 && !token_keep) || !cu_seqlens || !kept_index || !new_cu_seqlens || !new_seq_lens ||
+        !num_actual_tokens || !dev_status)
         return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31)) return UP_ERR_ARG;
     if (T > UP_NOALLOC_MAX_TOKENS) return UP_ERR_WORKSPACE;     // beyond the fixed scratch: use up_compact

@@ -91,9 +91,10 @@ using namespace up;
 extern "C" up_status up_slot_mapping(const int64_t* positions, const int32_t* cu_seqlens, int R, int64_t T_upper,
                                      const int32_t* num_tokens, const int32_t* block_table, int max_blocks, int B,
                                      int64_t* slots, int32_t* dev_status, void* stream) {
-    if (!positions || !cu_seqlens || !block_table || !slots || !dev_status) return UP_ERR_ARG;
+    if (!cu_seqlens || !block_table || !dev_status) return UP_ERR_ARG;
     if (R <= 0 || T_upper < 0 || max_blocks <= 0 || B <= 0) return UP_ERR_ARG;
-    if (T_upper == 0) return UP_OK;
+    if (T_upper == 0) return UP_OK;        // no tokens: positions and slots may be empty (NULL)
+    if (!positions || !slots) return UP_ERR_ARG;
     const int grid = static_cast<int>(std::min<int64_t>(cdiv(T_upper, 256), 8 * num_sms()));
     launch_pdl(meta::slot_kernel, dim3(grid), dim3(256), 0, static_cast<cudaStream_t>(stream),
         positions, cu_seqlens, R, T_upper, num_tokens, block_table, max_blocks, B, slots, dev_status);

@@ -1092,7 +1092,8 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
                                      const int32_t* cu_blocks, int64_t nb_cap, float* block_scores,
                                      float* token_scores, void* ws, size_t ws_bytes, int32_t* dev_status,
                                      void* stream) {
-    if (!Q || !K || !cu_seqlens || !cu_blocks || !block_scores || !ws || !dev_status) return UP_ERR_ARG;
+    // Q and K may be NULL for a batch without tokens (T = 0): nothing is read from them
+    if ((T > 0 && (!Q || !K)) || !cu_seqlens || !cu_blocks || !block_scores || !ws || !dev_status) return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || nb_cap < 0 || !(sm_scale > 0.f) || !isfinite(sm_scale))
         return UP_ERR_ARG;
     Geometry g;

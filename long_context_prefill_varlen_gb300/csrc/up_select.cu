@@ -300,7 +300,8 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
                                     int R, int64_t T, int64_t nb_cap, int G, int n, int A, double p,
                                     uint8_t* block_keep, uint8_t* token_keep, int32_t* kstar, int32_t* dev_status,
                                     void* stream) {
-    if (!block_scores || !cu_blocks || !cu_seqlens || !block_keep || !token_keep || !kstar || !dev_status)
+    // token_keep may be NULL for a batch without tokens (T = 0)
+    if (!block_scores || !cu_blocks || !cu_seqlens || !block_keep || (T > 0 && !token_keep) || !kstar || !dev_status)
         return UP_ERR_ARG;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || nb_cap < 0 || G <= 0 || n < 1 || A < 0) return UP_ERR_ARG;
     if (!(p > 0.0) || !(p <= 1.0)) return UP_ERR_ARG;
