@@ -10,7 +10,8 @@ d_k 128, hidden 4096, G 64, n 128, A 128, p 0.99), synthetic seeded bf16 inputs.
 flushed (512 MB write) before every timed step.  `--impl reference` times the fp64 CPU oracle
 on the host cores instead (bounded sample of the same workload per step).  `--sweep rho|ablation`
 prints measured sweeps instead of the step line (compaction against the kept fraction; the stages
-over G, n and p).
+over G, n and p); `--sweep stack` times a random-weight decoder stack with one drop against the top-p
+threshold (the saving of Eqs. 7-10).
 """
 from __future__ import annotations
 
@@ -45,9 +46,13 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--p", type=float, default=None, help="override the workload's top-p threshold")
-    ap.add_argument("--sweep", choices=["rho", "ablation"], default=None,
+    ap.add_argument("--sweep", choices=["rho", "ablation", "stack"], default=None,
                     help="instead of the step line, one JSON line per point: 'rho' = compaction and scatter "
-                         "bandwidth against the kept fraction; 'ablation' = the step's stages over G, n and p")
+                         "bandwidth against the kept fraction; 'ablation' = the step's stages over G, n and p; "
+                         "'stack' = a random-weight decoder stack with one drop, against the top-p threshold")
+    ap.add_argument("--stack-layers", type=int, default=32, help="layers of the --sweep stack decoder stack")
+    ap.add_argument("--drop-layer", type=int, default=10, help="0-based layer of the --sweep stack drop")
+    ap.add_argument("--stack-ffn", type=int, default=14336, help="FFN width of the --sweep stack layers")
     return ap.parse_args()
 
 
@@ -430,6 +435,9 @@ def run_sweep(args, w):
                               "scatter_frac_of_hbm": rows / (sms * 1e-3) / 1e9 / pk["hbm_gbs"],
                               "steps": steps, "peak_source": pk_kind}), flush=True)
         return
+    if args.sweep == "stack":
+        run_stack_sweep(args, w, dev, stream, pk, pk_kind)
+        return
     # ablation: G, n and p on the workload's geometry (the step's stages, eager, events between)
     inputs = sgpu.build_device(w, device=dev)
     cu = inputs["cu_seqlens"]
@@ -454,6 +462,51 @@ def run_sweep(args, w):
                                   "select_share": ms[1] / sum(ms), "steps": steps}), flush=True)
                 del step
                 torch.cuda.empty_cache()
+
+
+def run_stack_sweep(args, w, dev, stream, pk, pk_kind):
+    """The saving a drop buys on a decoder stack (Eqs. 7-10): an L-layer random-weight stack of the
+    workload's layer geometry over the workload's hidden states, without a drop and with one drop at
+    --drop-layer for several top-p thresholds; the forward's device time against the FLOPs accounting.
+    Every forward reads its weights (hundreds of MB per layer) from HBM, far beyond L2."""
+    import torch
+    from long_context_prefill_varlen_gb300 import layerstack as ls
+    from synth import gpu as sgpu
+    inputs = sgpu.build_device(w, device=dev, parts=("hidden", "positions"))
+    cu = inputs["cu_seqlens"]
+    g = ls.StackGeometry(d=w.hdim, Hq=w.Hq, Hkv=w.Hkv, dk=w.dk, ffn=args.stack_ffn)
+    L, l1 = args.stack_layers, args.drop_layer
+    stack = ls.RandomLlamaStack(L, g, seed=0, device=dev)
+    max_len = max(w.lengths)
+    steps = max(2, min(args.steps, 5))
+    base_ms = base_fl = None
+    for p in (None, 0.99, 0.95, 0.9, 0.75, 0.5):
+        drops = [] if p is None else [(l1, p)]
+        fwd = lambda: stack.forward(inputs["hidden"], inputs["positions"], cu, max_len, drops=drops, G=w.G, n=w.n,
+                                    A=w.A)
+        _, info = fwd()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            a.record(stream)
+            fwd()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = float(np.median([a.elapsed_time(b) for a, b in ev]))
+        kept = [int(x) for x in info[0]["step"].new_len.cpu().tolist()] if info else list(w.lengths)
+        fl = ls.stack_flops(w.lengths, g, L, [(l1, kept)] if info else [])
+        if p is None:
+            base_ms, base_fl = ms, fl
+        rec = {"sweep": "stack", "workload": w.name, "layers": L, "drop_layer": None if p is None else l1, "p": p,
+               "rho": sum(kept) / w.T, "ms_per_forward": ms, "prefill_tokens_per_s": w.T / (ms * 1e-3),
+               "speedup_vs_no_drop": base_ms / ms, "flops_ratio_no_drop_over_this": base_fl / fl,
+               "stack_tflops": fl / (ms * 1e-3) / 1e12,
+               "stack_frac_of_bf16_peak": fl / (ms * 1e-3) / 1e12 / pk["bf16_tflops_sustained"],
+               "steps": steps, "layers_are": "cuBLAS GEMMs + PyTorch varlen flash attention (random weights)",
+               "peak": "bf16_tflops_sustained", "peak_source": pk_kind}
+        print(json.dumps(rec), flush=True)
+        del info
+        torch.cuda.empty_cache()
 
 
 # ------------------------------------------------------------------------------------------ report
