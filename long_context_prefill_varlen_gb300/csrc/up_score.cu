@@ -18,11 +18,12 @@
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
 //   warp 1     TMEM allocator and tcgen05.mma issuer of the even jobs; warp 18 issues the odd jobs
 //              (all three run their loop on the whole warp and issue from one elected lane)
-//   warps 2-17 four epilogue warpgroups.  A job is one 128x128 fp32 accumulator; with J jobs per
-//              key tile, warpgroup g takes jobs g, g+4, ... when J >= 3, half a job (64 columns) when
-//              J = 2 and a quarter (32 columns) when J = 1.  TMEM is read in 16-column chunks, the
-//              next chunk's load in flight while the current one is reduced.
-// TMEM: 4 accumulators of 128 columns (the whole 512-column TMEM), used as a ring of jobs.
+//   warps 2-17 four epilogue warpgroups.  A job is one 128 x W fp32 accumulator (W = 128 query rows;
+//              W = 256 in pass 2 when the slab has 256 rows); with J jobs per key tile,
+//              warpgroup g takes jobs g, g+4, ... when J >= 3, half a job when J = 2 and a quarter
+//              when J = 1.  TMEM is read in 16-column chunks, the next chunk's load in flight while
+//              the current one is reduced.
+// TMEM: the whole 512 columns, a ring of 4 (W = 128) or 2 (W = 256) accumulators.
 // Per element the epilogue spends one ex2 on the SFU (32/clk/SM on this part, the same rate at
 // which the tensor core produces S elements at d_k = 128) plus one FFMA and one FADD.
 #include <math.h>
@@ -48,6 +49,7 @@ constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
 constexpr int kMaxJ = 8;                        // 128-row jobs per slab (d_k = 64 -> 8)
 constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
+constexpr uint32_t kIdescWide = idesc_bf16_f32(128, 256);
 constexpr int kCtrlBytes = 256;
 constexpr int kCvecFloats = 1024;
 constexpr int kXchgBytes = 4 * 2 * 128 * 8;     // pass 1: (m,l) of 4 warpgroups x 2 jobs
@@ -66,6 +68,7 @@ struct Params {
     const int32_t* cu;
     const int32_t* cb;
     int R, T, Hq, Hkv, dk, G, n, group, rows_total, slab_rows, slabs, J, box_rows, units_per_req;
+    int wide2;             // pass 2 takes one 256-row job per key tile (J = 2)
     float a;
     int64_t nb_cap;
     int4* items;
@@ -79,6 +82,25 @@ struct Params {
     float* token_scores;
     int32_t* status;
 };
+
+// Jobs of one key tile in a pass: J jobs of W query rows (one 128 x W fp32 accumulator each, W TMEM
+// columns) in a ring of nbuf = 512 / W TMEM buffers, wpj warpgroups draining each job (W / wpj
+// columns each).  Pass 1 keeps W = 128 (a query row per TMEM lane).  Pass 2 puts keys in the lanes,
+// and with a 256-row slab (J = 2: d_k = 256, or 256 window rows per KV head) it takes one job of
+// W = 256 per tile, drained by all four warpgroups: a 128 x 256 x 16 MMA reads 12 KB of shared
+// memory in 128 cycles (96 B per clock), where two 128 x 128 x 16 MMAs read 16 KB, the whole 128 B
+// per clock, and the TMA writes of the K tiles wait for gaps.  Measured on the score call: 7-8%
+// faster at d_k = 256; with the 512-row slab of d_k = 128 (two 256-row jobs) 1-4% slower than four
+// 128-row jobs, whose TMEM buffers come free sooner, so J = 4 keeps W = 128.
+struct JobMap {
+    int J, W, nbuf, nb_log, wpj;
+};
+__host__ __device__ constexpr int wg_per_job(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
+template <int PASS>
+__host__ __device__ __forceinline__ JobMap job_map(const Params& P) {
+    if (PASS == 2 && P.wide2) return JobMap{P.J / 2, 256, 2, 1, 4};
+    return JobMap{P.J, 128, 4, 2, wg_per_job(P.J)};
+}
 
 static bool geometry(int Hq, int Hkv, int dk, int n, Geometry* g) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
@@ -360,7 +382,9 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
     volatile int* abort_flag = S.abort_flag;
     int prev_unit = -1;
     uint32_t stage_cnt = 0, slab_cnt = 0, jc = 0;
-    const int J = P.J;
+    const JobMap jm = job_map<PASS>(P);
+    const int J = jm.J;
+    const uint32_t idesc = jm.W == 256 ? kIdescWide : kIdesc;
     // base descriptors: query slab at (chunk 0, row 0) and K stage 0; strides in bytes
     const uint64_t slab_d0 = sdesc_sw128(smem_u32(S.slab));
     const uint64_t stage_d0 = sdesc_sw128(smem_u32(S.stages));
@@ -390,12 +414,12 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                 // jobs outer: the tile's K stages stay resident while the J jobs run
                 bool landed = false;
                 for (int j = 0; j < J; ++j) {
-                    const uint32_t q = jc + j, buf = q & 3;
+                    const uint32_t q = jc + j, buf = q & (jm.nbuf - 1);
                     if (!mine(q)) continue;
-                    if (!wait_all(smem_u32(S.tempty + buf), ((q >> 2) & 1) ^ 1)) goto out;
+                    if (!wait_all(smem_u32(S.tempty + buf), ((q >> jm.nb_log) & 1) ^ 1)) goto out;
                     tc_fence_after();
-                    const uint64_t qd = desc_add(slab_d0, j * 128 * 128);
-                    const uint32_t d_tmem = tmem_base + buf * 128;
+                    const uint64_t qd = desc_add(slab_d0, j * jm.W * 128);
+                    const uint32_t d_tmem = tmem_base + buf * jm.W;
 #pragma unroll
                     for (int c = 0; c < NC; ++c) {
                         const uint32_t sc = stage_cnt + c, s = sc % kStages;
@@ -409,7 +433,7 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                         for (int k = 0; k < 4; ++k) {
                             const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
                             const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
-                            if (leader) tc_mma_bf16(d_tmem, a, b, kIdesc, (c | k) != 0);
+                            if (leader) tc_mma_bf16(d_tmem, a, b, idesc, (c | k) != 0);
                         }
                     }
                     landed = true;
@@ -427,7 +451,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                 // chunks outer (d_k = 256, J <= 2): each K stage is released as soon as all jobs used it
                 for (int j = 0; j < J; ++j) {
                     const uint32_t q = jc + j;
-                    if (mine(q) && !wait_all(smem_u32(S.tempty + (q & 3)), ((q >> 2) & 1) ^ 1)) goto out;
+                    if (mine(q) && !wait_all(smem_u32(S.tempty + (q & (jm.nbuf - 1))), ((q >> jm.nb_log) & 1) ^ 1))
+                        goto out;
                 }
                 tc_fence_after();
 #pragma unroll
@@ -438,20 +463,20 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                     const uint64_t kd = desc_add(stage_d0, s * kStageBytes);
                     for (int j = 0; j < J; ++j) {
                         if (!mine(jc + j)) continue;
-                        const uint32_t d_tmem = tmem_base + ((jc + j) & 3) * 128;
-                        const uint64_t qdc = desc_add(slab_d0, j * 128 * 128 + c * slab_chunk_bytes);
+                        const uint32_t d_tmem = tmem_base + ((jc + j) & (jm.nbuf - 1)) * jm.W;
+                        const uint64_t qdc = desc_add(slab_d0, j * jm.W * 128 + c * slab_chunk_bytes);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
                             const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
                             const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
-                            if (leader) tc_mma_bf16(d_tmem, a, b, kIdesc, (c | k) != 0);
+                            if (leader) tc_mma_bf16(d_tmem, a, b, idesc, (c | k) != 0);
                         }
                     }
                     commit(smem_u32(S.empty + s));
                     ++stage_cnt;
                 }
                 for (int j = 0; j < J; ++j)
-                    if (mine(jc + j)) commit(smem_u32(S.tfull + ((jc + j) & 3)));
+                    if (mine(jc + j)) commit(smem_u32(S.tfull + ((jc + j) & (jm.nbuf - 1))));
                 jc += J;
             }
         }
@@ -466,12 +491,11 @@ out:
     }
 }
 
-// Job map of the epilogue (one place for both the dispatch and the epilogue): with J jobs per key
-// tile, wg_per_job(J) warpgroups share a job (each reads chunks_per_slice(J) 16-column chunks of it)
-// and warpgroup g takes the jobs g / wpj + u * (4 / wpj).  (Splitting J = 4 jobs over pairs of
-// warpgroups, so that each pair alternates between two TMEM buffers, measured slower: the per-job
-// overheads doubled.)
-__host__ __device__ constexpr int wg_per_job(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
+// Job map of the epilogue (one place for both the dispatch and the epilogue): with J jobs of W rows
+// per key tile and wpj warpgroups on each job (job_map), each warpgroup reads W / 16 / wpj 16-column
+// chunks of a job (chunks_per_slice(J) for W = 128) and warpgroup g takes the jobs
+// g / wpj + u * (4 / wpj).  (Splitting J = 4 jobs of 128 rows over pairs of warpgroups, so that each
+// pair alternates between two TMEM buffers, measured slower: the per-job overheads doubled.)
 __host__ __device__ constexpr int chunks_per_slice(int J) { return 8 / wg_per_job(J); }
 static_assert(chunks_per_slice(1) == 2 && chunks_per_slice(2) == 4 && chunks_per_slice(3) == 8 &&
                   chunks_per_slice(4) == 8 && chunks_per_slice(8) == 8,
@@ -705,9 +729,10 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
     const int q = warp & 3;                     // TMEM lane quarter this warp may access
     const int rl = q * 32 + lane;               // row (pass 1) or key (pass 2) inside a 128-tile
     const float a = P.a;
-    const int J = P.J;
-    const int wpj = wg_per_job(J);              // warpgroups per job
-    const int cols = NCH * 16;                  // columns this warpgroup reads per job = 128 / wpj
+    const JobMap jm = job_map<PASS>(P);
+    const int J = jm.J;
+    const int wpj = jm.wpj;                     // warpgroups per job
+    const int cols = NCH * 16;                  // columns this warpgroup reads per job = W / wpj
     const int col0 = (wpj == 1 ? 0 : (wg % wpj) * cols);
     const int jfirst = wg / wpj;
     const int jstep = 4 / wpj;
@@ -750,12 +775,12 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
             int u = 0;
             for (int j = jfirst; j < J; j += jstep, ++u) {
                 const uint32_t jc = tiles_done * J + j;
-                const uint32_t buf = jc & 3;
+                const uint32_t buf = jc & (jm.nbuf - 1);
                 const bool ok =
-                    __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (jc >> 2) & 1, abort_flag));
+                    __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (jc >> jm.nb_log) & 1, abort_flag));
                 tc_fence_after();
-                const uint32_t ta = tl + buf * 128;
-                const float* ncv0 = S.cvec + j * 128 + col0;
+                const uint32_t ta = tl + buf * jm.W;
+                const float* ncv0 = S.cvec + j * jm.W + col0;
                 float mm = u ? m1 : m0, ll = u ? l1 : l0;
                 bool rvalid = false;
                 int lim0 = 0;
@@ -772,7 +797,7 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                     run_job_fast<PASS, NCH>(S, ta, buf, lane, a, ncv0, mm, ll, acc);
                 else
                     run_job_slow<PASS>(S, ta, buf, lane, ok, NCH, a, rvalid, lim0, ncv0, kt * kTileKeys + rl,
-                                       row0 + j * 128 + col0, P.n, I.N, P.rows_total, mm, ll, acc);
+                                       row0 + j * jm.W + col0, P.n, I.N, P.rows_total, mm, ll, acc);
                 if (PASS == 1) {
                     if (u) { m1 = mm; l1 = ll; } else { m0 = mm; l0 = ll; }
                 }
@@ -903,7 +928,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(S.tfull + b), 1);
             // one arrival per epilogue warp that reads the job: 4 warps per warpgroup on it
-            mbar_init(smem_u32(S.tempty + b), 4 * wg_per_job(P.J));
+            mbar_init(smem_u32(S.tempty + b), 4 * job_map<PASS>(P).wpj);
         }
         mbar_init(smem_u32(S.slab_full), 1);
         mbar_init(smem_u32(S.slab_free), kIssuers);
@@ -942,7 +967,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp == kIssuer1Warp) {
         mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : 1u);
     } else {
-        switch (chunks_per_slice(P.J)) {         // 16-column chunks per job slice
+        const JobMap jm = job_map<PASS>(P);
+        switch (jm.W / 16 / jm.wpj) {            // 16-column chunks per job slice
             case 8: epilogue<PASS, 8>(P, S, tmem_base, it0, it1); break;
             case 4: epilogue<PASS, 4>(P, S, tmem_base, it0, it1); break;
             default: epilogue<PASS, 2>(P, S, tmem_base, it0, it1); break;
@@ -1120,6 +1146,7 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.slab_rows = g.slab_rows;
     P.slabs = g.slabs;
     P.J = g.J;
+    P.wide2 = g.J == 2 ? 1 : 0;
     P.box_rows = g.box_rows;
     P.units_per_req = Hkv * g.slabs;
     P.a = sm_scale * 1.4426950408889634f;
