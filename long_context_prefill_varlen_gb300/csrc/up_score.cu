@@ -69,6 +69,7 @@ struct Params {
     const int32_t* cb;
     int R, T, Hq, Hkv, dk, G, n, group, rows_total, slab_rows, slabs, J, box_rows, units_per_req;
     int wide2;             // pass 2 takes one 256-row job per key tile (J = 2)
+    int sync_slabs;        // slabs > 1: CTA groups walk the same key tiles, one slab each (see plan)
     float a;
     int64_t nb_cap;
     int4* items;
@@ -209,19 +210,31 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         off += ni * P.units_per_req;
     }
     __syncthreads();
-    // every thread writes items: item `it` belongs to the largest request r whose first item is <= it
+    // Items are listed slab-major: all items of query slab 0 in (request, KV head, key tiles) order,
+    // then the same sequence for slab 1, and so on.  Every (request, KV head, tile pair) has one item
+    // per slab, so the S = slabs runs are equally long and item s * (total / S) + i is item i of
+    // run 0 with slab s.  With sync_slabs the CTAs come in S sets that split the runs identically
+    // (score_pass_kernel), so the S CTAs holding the slabs of a KV head walk the same key tiles side by
+    // side and each K tile is read from DRAM about once, the other S - 1 reads hitting L2.  Unit u's
+    // items are therefore not contiguous in the list; its pass-1 partials are indexed by the item's
+    // tile pair inside the unit (unit_items[u].x + pair).  With one slab this is the plain order.
+    const int S = P.slabs;
+    const int run = total / S;
     for (int it = tid; it < total; it += blockDim.x) {
+        const int sl = it / run, rel = it - sl * run;
+        // the request: the largest r whose first run-0 item (its first item / S) is <= rel; never an
+        // empty request (an empty request shares its first item with the next one, and rel < run
+        // excludes an empty last request)
         int lo = 0, hi = P.R;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (P.unit_items[mid * P.units_per_req].x <= it) lo = mid; else hi = mid;
+            if (P.unit_items[mid * P.units_per_req].x / S <= rel) lo = mid; else hi = mid;
         }
-        // the largest r with first_item(r) <= it is never an empty request (an empty request shares its
-        // first item with the next one, and it < total excludes an empty last request)
         const int r = lo;
         const int ni = nitems(r);
-        const int rel = it - P.unit_items[r * P.units_per_req].x;
-        const int kk = rel / ni, sidx = rel % ni;
+        const int rel2 = rel - P.unit_items[r * P.units_per_req].x / S;
+        const int kh = rel2 / ni, sidx = rel2 % ni;
+        const int kk = kh * S + sl;
         const int N = P.cu[r + 1] - P.cu[r];
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
         P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
@@ -839,7 +852,7 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
             // merge the warpgroups that share a job (fixed order), write this item's partial (m, l)
             // into the unit's block, laid out [row][item of the unit] for the merge kernel
             const int2 ui = P.unit_items[I.unit];
-            float2* part = P.ml + (size_t)ui.x * P.slab_rows + (it - ui.x);
+            float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;   // tile pair in the unit
             float2* xm = reinterpret_cast<float2*>(S.xchg);             // [4 warpgroups][2 jobs][128 rows]
             if (wpj > 1) {
                 int u = 0;
@@ -959,8 +972,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (PASS == 1) pdl_wait();
     pdl_trigger();
     const int n_items = uni(__ldcg(P.n_items));
-    const int it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
-    const int it1 = static_cast<int>((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    int it0, it1;
+    if (P.sync_slabs) {
+        // gridDim.x = S * groups: CTA (slab s, group g) takes the g-th share of slab s's run
+        const int groups = gridDim.x / P.slabs, run = n_items / P.slabs;
+        const int sl = blockIdx.x / groups, g = blockIdx.x % groups;
+        it0 = sl * run + static_cast<int>((int64_t)g * run / groups);
+        it1 = sl * run + static_cast<int>((int64_t)(g + 1) * run / groups);
+    } else {
+        it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
+        it1 = static_cast<int>((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    }
 
     if (warp == 0) {
         producer<NC>(P, S, &tmQ, &tmK, it0, it1);
@@ -1168,7 +1190,11 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     if (T > 0) {
         CUtensorMap tq, tk;
         if (!make_map(&tq, Q, T, Hq, dk, g.box_rows) || !make_map(&tk, K, T, Hkv, dk, kTileKeys)) return UP_ERR_CUDA;
-        const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items_cap)));
+        int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items_cap)));
+        if (g.slabs > 1 && grid >= g.slabs) {
+            grid = grid / g.slabs * g.slabs;
+            P.sync_slabs = 1;
+        }
         cudaError_t e;
         const int64_t merge_rows = L.units * g.slab_rows;
         switch (g.nc) {
