@@ -69,7 +69,7 @@ struct Params {
     const int32_t* cb;
     int R, T, Hq, Hkv, dk, G, n, group, rows_total, slab_rows, slabs, J, box_rows, units_per_req;
     int wide2;             // pass 2 takes one 256-row job per key tile (J = 2)
-    int sync_slabs;        // slabs > 1: CTA groups walk the same key tiles, one slab each (see plan)
+    int nsets;             // CTA sets that walk the same key tiles side by side (see plan)
     float a;
     int64_t nb_cap;
     int4* items;
@@ -118,6 +118,15 @@ static bool geometry(int Hq, int Hkv, int dk, int n, Geometry* g) {
     g->box_rows = std::min(n, 128);
     g->nc = dk / 64;
     return g->J <= kMaxJ && (g->nc < 4 || g->J <= 2);
+}
+
+// CTA sets of the score passes: every unit of a request (KV heads x slabs) when that many sets leave
+// at most 2% of the SMs idle, else the slabs of a KV head under the same rule, else one set.
+static int work_sets(int units_per_req, int slabs, int sms) {
+    auto fits = [&](int s) { return s <= sms && (sms % s) * 50 <= sms; };
+    if (units_per_req > 1 && fits(units_per_req)) return units_per_req;
+    if (slabs > 1 && fits(slabs)) return slabs;
+    return 1;
 }
 
 static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_cap, bool tok) {
@@ -210,31 +219,33 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         off += ni * P.units_per_req;
     }
     __syncthreads();
-    // Items are listed slab-major: all items of query slab 0 in (request, KV head, key tiles) order,
-    // then the same sequence for slab 1, and so on.  Every (request, KV head, tile pair) has one item
-    // per slab, so the S = slabs runs are equally long and item s * (total / S) + i is item i of
-    // run 0 with slab s.  With sync_slabs the CTAs come in S sets that split the runs identically
-    // (score_pass_kernel), so the S CTAs holding the slabs of a KV head walk the same key tiles side by
-    // side and each K tile is read from DRAM about once, the other S - 1 reads hitting L2.  Unit u's
-    // items are therefore not contiguous in the list; its pass-1 partials are indexed by the item's
-    // tile pair inside the unit (unit_items[u].x + pair).  With one slab this is the plain order.
-    const int S = P.slabs;
-    const int run = total / S;
+    // Items are listed set-major.  Unit kk of a request (KV head kh, query slab sl, kk = kh * slabs +
+    // sl) belongs to set kk % nsets; the list holds all items of set 0 in (request, kk / nsets, tile
+    // pair) order, then the same sequence for set 1, and so on.  Every (request, tile pair) has an
+    // item in each unit, so the nsets runs are equally long and item s * run + i is item i of run 0
+    // moved to set s.  The score passes split every run identically over nsets sets of CTAs, so the
+    // CTAs holding the units of one request walk the same key tiles side by side: with nsets = slabs
+    // a K tile is read from DRAM about once instead of once per slab, and with nsets = Hkv * slabs the
+    // KV heads of a token range are also read together (whole rows of the [T, Hkv, d_k] K tensor).
+    // A unit's items are therefore not contiguous in the list; its pass-1 partials are indexed by the
+    // item's tile pair inside the unit (unit_items[u].x + pair).  nsets = 1 is the plain order.
+    const int NS = P.nsets;
+    const int run = total / NS;
     for (int it = tid; it < total; it += blockDim.x) {
-        const int sl = it / run, rel = it - sl * run;
-        // the request: the largest r whose first run-0 item (its first item / S) is <= rel; never an
+        const int set = it / run, rel = it - set * run;
+        // the request: the largest r whose first run-0 item (its first item / NS) is <= rel; never an
         // empty request (an empty request shares its first item with the next one, and rel < run
         // excludes an empty last request)
         int lo = 0, hi = P.R;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (P.unit_items[mid * P.units_per_req].x / S <= rel) lo = mid; else hi = mid;
+            if (P.unit_items[mid * P.units_per_req].x / NS <= rel) lo = mid; else hi = mid;
         }
         const int r = lo;
         const int ni = nitems(r);
-        const int rel2 = rel - P.unit_items[r * P.units_per_req].x / S;
-        const int kh = rel2 / ni, sidx = rel2 % ni;
-        const int kk = kh * S + sl;
+        const int rel2 = rel - P.unit_items[r * P.units_per_req].x / NS;
+        const int kq = rel2 / ni, sidx = rel2 % ni;
+        const int kk = kq * NS + set;
         const int N = P.cu[r + 1] - P.cu[r];
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
         P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
@@ -973,15 +984,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     pdl_trigger();
     const int n_items = uni(__ldcg(P.n_items));
     int it0, it1;
-    if (P.sync_slabs) {
-        // gridDim.x = S * groups: CTA (slab s, group g) takes the g-th share of slab s's run
-        const int groups = gridDim.x / P.slabs, run = n_items / P.slabs;
-        const int sl = blockIdx.x / groups, g = blockIdx.x % groups;
-        it0 = sl * run + static_cast<int>((int64_t)g * run / groups);
-        it1 = sl * run + static_cast<int>((int64_t)(g + 1) * run / groups);
-    } else {
-        it0 = static_cast<int>((int64_t)blockIdx.x * n_items / gridDim.x);
-        it1 = static_cast<int>((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
+    {
+        // gridDim.x = nsets * groups: CTA (set s, group g) takes the g-th share of set s's run
+        const int groups = gridDim.x / P.nsets, run = n_items / P.nsets;
+        const int set = blockIdx.x / groups, g = blockIdx.x % groups;
+        it0 = set * run + static_cast<int>((int64_t)g * run / groups);
+        it1 = set * run + static_cast<int>((int64_t)(g + 1) * run / groups);
     }
 
     if (warp == 0) {
@@ -1183,6 +1191,7 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.block_scores = block_scores;
     P.token_scores = token_scores;
     P.status = dev_status;
+    P.nsets = work_sets(P.units_per_req, g.slabs, num_sms());
 
     cudaError_t le = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, P);
     count_launch();
@@ -1191,10 +1200,7 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
         CUtensorMap tq, tk;
         if (!make_map(&tq, Q, T, Hq, dk, g.box_rows) || !make_map(&tk, K, T, Hkv, dk, kTileKeys)) return UP_ERR_CUDA;
         int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items_cap)));
-        if (g.slabs > 1 && grid >= g.slabs) {
-            grid = grid / g.slabs * g.slabs;
-            P.sync_slabs = 1;
-        }
+        grid = grid / P.nsets * P.nsets;
         cudaError_t e;
         const int64_t merge_rows = L.units * g.slab_rows;
         switch (g.nc) {
