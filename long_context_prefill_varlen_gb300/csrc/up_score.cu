@@ -894,8 +894,8 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
     }
 }
 
-// Fold each query row's pass-1 partials (one per work item of its unit, in item order) into
-// c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
+// Fold each query row's pass-1 partials (one per work item of its unit, in the unit's key-tile order)
+// into c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
 __global__ void __launch_bounds__(256) merge_kernel(Params P) {
     pdl_wait();
     pdl_trigger();
