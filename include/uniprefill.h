@@ -146,6 +146,9 @@ up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,
  *   {(l_k, s_k^r)} of [UP 3.5] (both optional; kept_len int32 [L, R], drop_layer u8 [L]).
  * hdim % 8 == 0; hidden/out_hidden 16-byte aligned; token_keep 16-byte aligned (may be NULL when
  * T = 0, as may hidden/positions/slots and their outputs).
+ * cu_seqlens that is not a non-decreasing 0..T sequence sets UP_DEV_BAD_CU_SEQLENS in dev_status and
+ * num_actual_tokens = 0, and leaves new_cu_seqlens, new_seq_lens and the drop history unwritten;
+ * kept_index and the gathered rows, which do not depend on cu_seqlens, are still written.
  * ws: up_compact_workspace_bytes(R, T) bytes. */
 up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seqlens, int R, int64_t T,
                      const uint16_t* hidden, int hdim, const int64_t* positions, const int64_t* slots,

@@ -116,12 +116,13 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
         if ((r == 0 && c0 != 0) || c1 < c0 || c1 > T || (r == R - 1 && c1 != T)) s_bad = 1;
     }
     __syncthreads();
-    if (s_bad) {
-        if (tid == 0) {
-            set_status(status, UP_DEV_BAD_CU_SEQLENS);
-            *num_actual = 0;
-        }
-        return;
+    // Invalid cu_seqlens: reported, num_actual_tokens = 0 and no per-request metadata.  The tile
+    // offsets depend only on the mask and T, so they are still computed: the gather launched after
+    // this kernel reads them and stays in bounds whatever cu_seqlens holds.
+    const bool bad = s_bad != 0;
+    if (bad && tid == 0) {
+        set_status(status, UP_DEV_BAD_CU_SEQLENS);
+        *num_actual = 0;
     }
     const int tiles = (T + kTile - 1) / kTile;
     if (count_here) {
@@ -167,6 +168,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
         off += tile_cnt[i];
     }
     __syncthreads();
+    if (bad) return;
     // kept tokens before each request boundary: one warp per boundary
     for (int r = w; r <= R; r += blockDim.x / 32) {
         const int x0 = cu[r];

@@ -261,6 +261,30 @@ def test_bad_cu_seqlens_is_reported_not_faulted():
     assert up.up_read_status(step.status) == 1
 
 
+def test_bad_cu_seqlens_in_compaction_is_reported_and_stays_in_bounds():
+    """Non-monotone cu_seqlens: up_compact reports UP_DEV_BAD_CU_SEQLENS and sets num_actual_tokens = 0;
+    the token-side outputs, which do not depend on cu_seqlens, are the stable compaction of the mask."""
+    w = recipe.small(lengths=(1500, 700, 900), Hq=4, Hkv=2, dk=128, hdim=64, salt=5)
+    host = gen.materialize(w)
+    d = sgpu.to_device(host)
+    step = up.DropStep(d["cu_seqlens"], w.T, w.Hq, w.Hkv, w.dk, w.hdim, G=w.G, n=w.n)
+    keep = (np.random.default_rng(5).random(w.T) < 0.6).astype(np.uint8)
+    step.token_keep.copy_(torch.from_numpy(keep).cuda())
+    step.cu.copy_(_i32([0, 1600, 1500, w.T]))     # non-monotone
+    step.compact(d["hidden"], d["positions"], d["slots"])
+    torch.cuda.synchronize()
+    assert up.up_read_status(step.status) == 1
+    assert int(step.num_actual.item()) == 0
+    ref = oracle.compact(keep, np.array([0, w.T], dtype=np.int32), host["hidden"], host["positions"],
+                         host["slots"])
+    Tp = ref["num_actual_tokens"]
+    got = parity.step_to_numpy(step)
+    assert np.array_equal(got["kept_index"][:Tp], ref["kept_index"])
+    assert np.array_equal(got["out_hidden"][:Tp], ref["hidden"])
+    assert np.array_equal(got["out_positions"][:Tp], ref["positions"])
+    assert np.array_equal(got["out_slots"][:Tp], ref["slots"])
+
+
 # ------------------------------------------------------------------------------------------ whole step
 
 def test_config1_end_to_end():
