@@ -182,9 +182,11 @@ up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t* cu_seqlen
 /* End-of-block carry-forward [UP 3.4, Eq. 8], in place:
  *   residual[kept_index[k], :] = new_states[k, :]  for k < *num_actual_tokens;
  *   rows of dropped tokens are not touched (they keep H^(b,0)).
- * new_states: bf16 [T_upper, hdim]; residual: bf16 [T_upper, hdim]; both 16-byte aligned (with
- * T_upper = 0 nothing is read or written and every pointer may be NULL);
- * hdim % 8 == 0.  kept_index/num_actual_tokens as produced by up_compact. */
+ * new_states: bf16 [T_upper, hdim], the compacted stream (T_upper >= *num_actual_tokens; a larger
+ * count is reported as UP_DEV_BAD_TOKEN_COUNT and nothing is copied); residual: bf16 [T, hdim], the
+ * full-length stream that up_compact compacted (every kept_index entry is below T); both 16-byte
+ * aligned (with T_upper = 0 nothing is read or written and every pointer may be NULL);
+ * hdim % 8 == 0.  kept_index/num_actual_tokens as produced by up_compact over that stream. */
 up_status up_scatter_back(const uint16_t* new_states, const int32_t* kept_index,
                           const int32_t* num_actual_tokens, int64_t T_upper, int hdim,
                           uint16_t* residual, int32_t* dev_status, void* stream);

@@ -178,8 +178,10 @@ def up_compact_noalloc(token_keep, cu_seqlens, kept_index, new_cu_seqlens, new_s
 
 
 def up_scatter_back(new_states, kept_index, num_actual_tokens, residual, dev_status, stream=None):
-    T_upper, hdim = residual.shape
-    assert new_states.shape[1] == hdim and new_states.shape[0] <= T_upper
+    """residual [T, hdim] receives the compacted rows new_states [T_upper <= T, hdim] (T_upper is
+    passed as the bound of *num_actual_tokens)."""
+    T, hdim = residual.shape
+    assert new_states.shape[1] == hdim and new_states.shape[0] <= T
     _check(load_library().up_scatter_back(_bf16(new_states), _p(kept_index), _p(num_actual_tokens),
                                           new_states.shape[0], hdim, _bf16(residual), _p(dev_status),
                                           _stream(stream)),
