@@ -188,6 +188,10 @@ SCORE_CASES = [
     (2, 1, 128, 64, 16, (50, 5, 0, 130)),
     (16, 8, 256, 64, 128, (2000, 513)),
     (8, 1, 64, 32, 1024, (3000, 1200)),
+    # the score passes' work order on 152 SMs: 16 units per request (2 slabs x 8 KV heads) do not
+    # divide the SMs, so the 2 slabs of a head form the CTA sets; 16 one-slab units, the plain order
+    (32, 8, 128, 64, 256, (1300, 600)),
+    (16, 16, 128, 64, 128, (900, 70, 1500)),
 ]
 
 
