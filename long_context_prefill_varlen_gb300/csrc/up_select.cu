@@ -109,55 +109,83 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     }
     __syncthreads();
 
-    // 2. four stable passes over the high word, ascending on ~key (= descending on key).  Warp w owns
-    //    positions [w*32*ipt, (w+1)*32*ipt), visited round by round (32 consecutive keys per round), so
-    //    (digit, warp, round, lane) order equals (digit, position) order: the passes are stable.
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int ps = 0; ps < 4; ++ps) {
-        const int shift = 32 + 8 * ps;
-        for (int i = tid; i < kRadix * kWarps; i += kThreads) hist[i] = 0;
-        __syncthreads();
-        uint32_t rank[kMaxIpt];
-        uint32_t dig[kMaxIpt];
-        const int base_k = warp * 32 * ipt + lane;
-#pragma unroll
-        for (int j = 0; j < kMaxIpt; ++j) {
-            if (j < ipt) {
-                const uint32_t d = static_cast<uint32_t>((~keys[base_k + 32 * j]) >> shift) & 0xFFu;
-                const uint32_t peers = __match_any_sync(0xffffffffu, d);
-                const uint32_t before = hist[d * kWarps + warp];
-                __syncwarp();
-                if ((peers & lt_mask) == 0) hist[d * kWarps + warp] = before + __popc(peers);
-                __syncwarp();
-                dig[j] = d;
-                rank[j] = before + __popc(peers & lt_mask);
+    if (ipt == 1) {
+        // 2a. at most kThreads blocks: a bitonic network over the whole 64-bit keys, one key per thread
+        //     (padding keys are 0 and sort last).  The keys are distinct (the block index is the low
+        //     word), so the descending order is the one the radix passes below produce.  Partners in
+        //     the same warp are exchanged by shuffle, the others through two alternating shared
+        //     buffers (one barrier per such step).
+        uint64_t v = keys[tid];
+        int par = 0;
+        for (int k = 2; k <= kThreads; k <<= 1) {
+            for (int j = k >> 1; j > 0; j >>= 1) {
+                uint64_t o;
+                if (j < 32) {
+                    o = __shfl_xor_sync(0xffffffffu, v, j);
+                } else {
+                    uint64_t* xb = alt + par * kThreads;
+                    xb[tid] = v;
+                    __syncthreads();
+                    o = xb[tid ^ j];
+                    par ^= 1;
+                }
+                const bool lower = (tid & j) == 0, desc = (tid & k) == 0;
+                v = (lower == desc) ? (v > o ? v : o) : (v < o ? v : o);
             }
         }
+        keys[tid] = v;
         __syncthreads();
-        // exclusive scan of hist in (digit, warp) order: 8 consecutive entries per thread
-        uint32_t loc[8];
-        uint32_t sum = 0;
+    } else {
+        // 2. four stable passes over the high word, ascending on ~key (= descending on key).  Warp w owns
+        //    positions [w*32*ipt, (w+1)*32*ipt), visited round by round (32 consecutive keys per round), so
+        //    (digit, warp, round, lane) order equals (digit, position) order: the passes are stable.
+        const uint32_t lt_mask = (1u << lane) - 1u;
+        for (int ps = 0; ps < 4; ++ps) {
+            const int shift = 32 + 8 * ps;
+            for (int i = tid; i < kRadix * kWarps; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            uint32_t rank[kMaxIpt];
+            uint32_t dig[kMaxIpt];
+            const int base_k = warp * 32 * ipt + lane;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            loc[e] = hist[tid * 8 + e];
-            sum += loc[e];
+            for (int j = 0; j < kMaxIpt; ++j) {
+                if (j < ipt) {
+                    const uint32_t d = static_cast<uint32_t>((~keys[base_k + 32 * j]) >> shift) & 0xFFu;
+                    const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                    const uint32_t before = hist[d * kWarps + warp];
+                    __syncwarp();
+                    if ((peers & lt_mask) == 0) hist[d * kWarps + warp] = before + __popc(peers);
+                    __syncwarp();
+                    dig[j] = d;
+                    rank[j] = before + __popc(peers & lt_mask);
+                }
+            }
+            __syncthreads();
+            // exclusive scan of hist in (digit, warp) order: 8 consecutive entries per thread
+            uint32_t loc[8];
+            uint32_t sum = 0;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                loc[e] = hist[tid * 8 + e];
+                sum += loc[e];
+            }
+            int tot;
+            uint32_t run = static_cast<uint32_t>(block_exclusive_scan<int>(static_cast<int>(sum), shi, &tot));
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const uint32_t c = loc[e];
+                hist[tid * 8 + e] = run;
+                run += c;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kMaxIpt; ++j)
+                if (j < ipt) alt[hist[dig[j] * kWarps + warp] + rank[j]] = keys[base_k + 32 * j];
+            __syncthreads();
+            uint64_t* t = keys;
+            keys = alt;
+            alt = t;
         }
-        int tot;
-        uint32_t run = static_cast<uint32_t>(block_exclusive_scan<int>(static_cast<int>(sum), shi, &tot));
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const uint32_t c = loc[e];
-            hist[tid * 8 + e] = run;
-            run += c;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < kMaxIpt; ++j)
-            if (j < ipt) alt[hist[dig[j] * kWarps + warp] + rank[j]] = keys[base_k + 32 * j];
-        __syncthreads();
-        uint64_t* t = keys;
-        keys = alt;
-        alt = t;
     }
     const int k0 = tid * ipt;      // from here on each thread owns a contiguous run of sorted positions
 
