@@ -4,10 +4,11 @@
 // and the drop-history record (section 3.5, "vLLM scheduler integration"), and the end-of-block
 // carry-forward of Eq. 8 (section 3.4).
 //
-// Compaction is three launches (two for streams of at most kScanCountTiles tiles), none of which
-// waits on another CTA:
-//   count   per 1024-token tile, the number of kept tokens (16-byte loads of the byte mask); for
-//           short streams the scan kernel counts the tiles itself
+// Compaction is three launches, none of which waits on another CTA (two for streams of at most
+// kScanCountTiles tiles, whose scan kernel counts the tiles itself, and one for streams of at most
+// kSelfScanTiles tiles, whose gather CTAs each count and scan the tiles; for longer streams that
+// repeated read of the mask by every CTA concentrated on a few L2 slices and slowed the step):
+//   count   per 1024-token tile, the number of kept tokens (16-byte loads of the byte mask)
 //   scan    one CTA: tile offsets, and per request prefix(cu[r]) = kept tokens before cu[r]
 //           -> new_cu_seqlens, new_seq_lens, num_actual_tokens, kept_len[layer], drop_layer[layer]
 //   gather  persistent CTAs over (tile, part) items, parts chosen so that there are several items per
@@ -32,6 +33,7 @@ constexpr int kRowUnroll = 8;
 constexpr int kGatherThreads = 256;
 constexpr int kMaxParts = 64;          // work items sharing one tile's row copies
 constexpr int kScanCountTiles = 64;    // up to this many tiles the scan kernel counts them itself
+constexpr int kSelfScanTiles = 8;      // up to this many tiles the gather scans the stream itself
 
 struct Layout {
     size_t tile_cnt, tile_off, total;
@@ -99,6 +101,52 @@ __global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __re
     if (threadIdx.x == 0) tile_cnt[blockIdx.x] = tot;
 }
 
+// Whether cu_seqlens is a non-decreasing 0..T sequence (all threads of the CTA take part; sh_bad is
+// a shared flag).
+__device__ __forceinline__ bool cu_valid(const int32_t* __restrict__ cu, int R, int T, int* sh_bad) {
+    if (threadIdx.x == 0) *sh_bad = 0;
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const int c0 = cu[r], c1 = cu[r + 1];
+        if ((r == 0 && c0 != 0) || c1 < c0 || c1 > T || (r == R - 1 && c1 != T)) *sh_bad = 1;
+    }
+    __syncthreads();
+    return *sh_bad == 0;
+}
+
+// The per-request side of the compaction, from the tile offsets (off[i] = kept tokens before tile i,
+// total = kept tokens of the stream): kept tokens before each request boundary (one warp per
+// boundary; the boundary's partial tile is counted flag by flag) -> new_cu_seqlens, new_seq_lens,
+// num_actual_tokens and the drop history.  Called by every thread of one CTA, cu_seqlens valid.
+__device__ void request_metadata(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu, int R, int tiles,
+                                 const int* off, int total, int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
+                                 int32_t* kept_len, uint8_t* drop_layer, int layer) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    for (int r = w; r <= R; r += nw) {
+        const int x0 = cu[r];
+        const int tile = x0 / kTile;
+        int c = 0;
+        for (int t = tile * kTile + lane; t < x0; t += 32) c += keep[t] != 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+        if (lane == 0) new_cu[r] = (tile < tiles ? off[tile] : total) + c;
+    }
+    __syncthreads();
+    for (int r = threadIdx.x; r < R; r += blockDim.x) {
+        const int len = new_cu[r + 1] - new_cu[r];
+        new_len[r] = len;
+        if (kept_len) kept_len[(int64_t)layer * R + r] = len;
+    }
+    if (threadIdx.x == 0) {
+        *num_actual = new_cu[R];
+        if (drop_layer) drop_layer[layer] = 1;
+    }
+}
+
+// Streams of more than kSelfScanTiles tiles: the tile counts (of count_kernel, or counted here for at
+// most kScanCountTiles tiles) -> tile offsets, and the per-request metadata.  Invalid cu_seqlens: reported, num_actual_tokens = 0 and no per-request
+// metadata; the tile offsets depend only on the mask and T, so they are still written and the gather
+// launched after this kernel stays in bounds whatever cu_seqlens holds.
 __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu,
                                                     int R, int T, int* tile_cnt, int* tile_off,
                                                     int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
@@ -109,18 +157,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
     __shared__ int sh[32];
     __shared__ int s_bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-    if (tid == 0) s_bad = 0;
-    __syncthreads();
-    for (int r = tid; r < R; r += blockDim.x) {
-        const int c0 = cu[r], c1 = cu[r + 1];
-        if ((r == 0 && c0 != 0) || c1 < c0 || c1 > T || (r == R - 1 && c1 != T)) s_bad = 1;
-    }
-    __syncthreads();
-    // Invalid cu_seqlens: reported, num_actual_tokens = 0 and no per-request metadata.  The tile
-    // offsets depend only on the mask and T, so they are still computed: the gather launched after
-    // this kernel reads them and stays in bounds whatever cu_seqlens holds.
-    const bool bad = s_bad != 0;
-    if (bad && tid == 0) {
+    const bool ok = cu_valid(cu, R, T, &s_bad);
+    if (!ok && tid == 0) {
         set_status(status, UP_DEV_BAD_CU_SEQLENS);
         *num_actual = 0;
     }
@@ -162,34 +200,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
         sh[lane] = s;
     }
     __syncthreads();
+    const int total = sh[31];
     int off = (w > 0 ? sh[w - 1] : 0) + x - local;
     for (int i = a0; i < a1; ++i) {
         tile_off[i] = off;
         off += tile_cnt[i];
     }
     __syncthreads();
-    if (bad) return;
-    // kept tokens before each request boundary: one warp per boundary
-    for (int r = w; r <= R; r += blockDim.x / 32) {
-        const int x0 = cu[r];
-        const int tile = x0 / kTile;
-        int c = 0;
-        for (int t = tile * kTile + lane; t < x0; t += 32) c += keep[t] != 0;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        const int before = (tile < tiles ? tile_off[tile] : (tiles > 0 ? tile_off[tiles - 1] + tile_cnt[tiles - 1] : 0)) + c;
-        if (lane == 0) new_cu[r] = before;
-    }
-    __syncthreads();
-    for (int r = tid; r < R; r += blockDim.x) {
-        const int len = new_cu[r + 1] - new_cu[r];
-        new_len[r] = len;
-        if (kept_len) kept_len[(int64_t)layer * R + r] = len;
-    }
-    if (tid == 0) {
-        *num_actual = new_cu[R];
-        if (drop_layer) drop_layer[layer] = 1;
-    }
+    if (!ok) return;
+    request_metadata(keep, cu, R, tiles, tile_off, total, new_cu, new_len, num_actual, kept_len, drop_layer, layer);
 }
 
 // One warp copies one row of V 16-byte vectors, kRowUnroll loads in flight per lane.
@@ -209,19 +228,70 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ s, uint4* __r
 // tile's kept tokens in ascending order (a scan of its 1024 flags, recomputed by every part), the
 // index/positions/slots rows written by part 0, and the part's contiguous share of the kept hidden rows
 // copied.
-template <bool ROWS>
+// Metadata outputs of a gather that scans the stream itself (SELF).
+struct MetaOut {
+    const int32_t* cu;
+    int R, layer;
+    int32_t *new_cu, *new_len, *num_actual, *kept_len, *status;
+    uint8_t* drop_layer;
+};
+
+// SELF (streams of at most kSelfScanTiles tiles, one launch for the whole compaction): every CTA
+// counts the tiles (one warp per tile) and scans the counts into shared memory instead of reading the
+// scan kernel's tile_off, and CTA 0 also validates cu_seqlens and writes the per-request metadata.
+template <bool ROWS, bool SELF>
 __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* __restrict__ keep, int T, int tiles,
                                                               int parts, const int* __restrict__ tile_off,
                                                               const int64_t* __restrict__ pos,
                                                               const int64_t* __restrict__ slots, int32_t* kept_index,
                                                               int64_t* out_pos, int64_t* out_slots,
                                                               const uint4* __restrict__ src, uint4* __restrict__ dst,
-                                                              int V) {
+                                                              int V, MetaOut M) {
     pdl_wait();
     pdl_trigger();
     __shared__ int s_src[kTile];           // source token of the tile's k-th kept token
     __shared__ int s_wsum[kTileThreads / 32];
+    __shared__ int s_off[kSelfScanTiles];
+    __shared__ int s_total, s_bad;
     const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+    if (SELF) {
+        for (int i = w; i < tiles; i += kGatherThreads / 32) {
+            int c = 0;
+            for (int j = lane; j < kTile / 16; j += 32) {
+                const int64_t t = (int64_t)i * kTile + j * 16;
+                if (t < T) c += count_nonzero_bytes(load_flags16(keep, t, T));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
+            if (lane == 0) s_off[i] = c;
+        }
+        __syncthreads();
+        if (w == 0) {                      // exclusive scan of <= 8 counts
+            const int x0 = 2 * lane < tiles ? s_off[2 * lane] : 0;
+            const int x1 = 2 * lane + 1 < tiles ? s_off[2 * lane + 1] : 0;
+            int x = x0 + x1;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            const int e = x - x0 - x1;
+            __syncwarp();
+            if (2 * lane < tiles) s_off[2 * lane] = e;
+            if (2 * lane + 1 < tiles) s_off[2 * lane + 1] = e + x0;
+            if (lane == 31) s_total = x;
+        }
+        __syncthreads();
+        if (blockIdx.x == 0) {
+            if (cu_valid(M.cu, M.R, T, &s_bad))
+                request_metadata(keep, M.cu, M.R, tiles, s_off, s_total, M.new_cu, M.new_len, M.num_actual,
+                                 M.kept_len, M.drop_layer, M.layer);
+            else if (tid == 0) {
+                set_status(M.status, UP_DEV_BAD_CU_SEQLENS);
+                *M.num_actual = 0;
+            }
+        }
+    }
     const int64_t items = (int64_t)tiles * parts;
     for (int64_t item = blockIdx.x; item < items; item += gridDim.x) {
         const int tile = static_cast<int>(item / parts), part = static_cast<int>(item % parts);
@@ -251,7 +321,7 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* _
 #pragma unroll
         for (int i = 0; i < kTileThreads / 32; ++i) cnt += s_wsum[i];
         __syncthreads();
-        const int base = tile_off[tile];
+        const int base = SELF ? s_off[tile] : tile_off[tile];
         if (part == 0) {
             for (int k = tid; k < cnt; k += kGatherThreads) {
                 const int sidx = s_src[k];
@@ -307,12 +377,34 @@ static int scatter_resident() {
 }
 
 // CTAs of gather_kernel that are resident on the whole GPU at once (occupancy x SMs), once per process.
-template <bool ROWS>
+template <bool ROWS, bool SELF>
 static int gather_resident() {
     static int n = 0;
     static std::once_flag once;
-    std::call_once(once, [] { n = resident_ctas(gather_kernel<ROWS>, kGatherThreads); });
+    std::call_once(once, [] { n = resident_ctas(gather_kernel<ROWS, SELF>, kGatherThreads); });
     return n;
+}
+
+template <bool SELF>
+static void launch_gather(const uint8_t* keep, int Ti, int tiles, const int* tile_off, const uint16_t* hidden,
+                          int hdim, const int64_t* positions, const int64_t* slots, uint16_t* out_hidden,
+                          int64_t* out_positions, int64_t* out_slots, int32_t* kept_index, const MetaOut& M,
+                          cudaStream_t st) {
+    // persistent CTAs: as many as fit on the GPU at once; parts per tile so that every resident CTA
+    // has several items (fine-grained enough that the last round is short)
+    const int resident = hidden ? gather_resident<true, SELF>() : gather_resident<false, SELF>();
+    const int parts = hidden ? static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxParts, cdiv(4 * resident, std::max(1, tiles)))))
+                             : 1;
+    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((int64_t)tiles * parts, resident)));
+    if (hidden)
+        launch_pdl(gather_kernel<true, SELF>, dim3(grid), dim3(kGatherThreads), 0, st,
+            keep, Ti, tiles, parts, tile_off, positions, slots, kept_index, out_positions, out_slots,
+            reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), hdim / 8, M);
+    else
+        launch_pdl(gather_kernel<false, SELF>, dim3(grid), dim3(kGatherThreads), 0, st,
+            keep, Ti, tiles, 1, tile_off, positions, slots, kept_index, out_positions, out_slots, nullptr,
+            nullptr, 0, M);
+    count_launch();
 }
 
 // The launches of one compaction, on the caller's workspace or the fixed scratch alike.
@@ -322,8 +414,14 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
                               int32_t* new_len, int32_t* num_actual, int32_t* kept_len, uint8_t* drop_layer,
                               int layer, int* tile_cnt, int* tile_off, int32_t* status, cudaStream_t st) {
     const int tiles = static_cast<int>(cdiv(Ti, kTile));
+    const MetaOut M{cu, R, layer, new_cu, new_len, num_actual, kept_len, status, drop_layer};
+    if (tiles <= kSelfScanTiles) {        // one launch: the gather scans the short stream itself
+        launch_gather<true>(keep, Ti, tiles, nullptr, hidden, hdim, positions, slots, out_hidden, out_positions,
+                            out_slots, kept_index, M, st);
+        return;
+    }
     const int count_here = tiles <= kScanCountTiles ? 1 : 0;
-    if (tiles > 0 && !count_here) {
+    if (!count_here) {
         launch_pdl(count_kernel, dim3(tiles), dim3(kTileThreads), 0, st, keep, Ti, tile_cnt);
         count_launch();
     }
@@ -331,22 +429,8 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
         keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len, drop_layer, layer, status,
         count_here);
     count_launch();
-    if (tiles == 0) return;
-    // persistent CTAs: as many as fit on the GPU at once; parts per tile so that every resident CTA
-    // has several items (fine-grained enough that the last round is short)
-    const int resident = hidden ? gather_resident<true>() : gather_resident<false>();
-    const int parts = hidden ? static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(kMaxParts, cdiv(4 * resident, tiles))))
-                             : 1;
-    const int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((int64_t)tiles * parts, resident)));
-    if (hidden)
-        launch_pdl(gather_kernel<true>, dim3(grid), dim3(kGatherThreads), 0, st, 
-            keep, Ti, tiles, parts, tile_off, positions, slots, kept_index, out_positions, out_slots,
-            reinterpret_cast<const uint4*>(hidden), reinterpret_cast<uint4*>(out_hidden), hdim / 8);
-    else
-        launch_pdl(gather_kernel<false>, dim3(grid), dim3(kGatherThreads), 0, st,
-            keep, Ti, tiles, 1, tile_off, positions, slots, kept_index, out_positions, out_slots, nullptr,
-            nullptr, 0);
-    count_launch();
+    launch_gather<false>(keep, Ti, tiles, tile_off, hidden, hdim, positions, slots, out_hidden, out_positions,
+                         out_slots, kept_index, M, st);
 }
 
 }  // namespace compact
