@@ -5,8 +5,11 @@ One step = one pass of the whole hot path over one batch:
   -> up_slot_mapping (Eq. 16, next layer) -> up_scatter_back (Eq. 8) -> up_seqused (Eq. 17)
 value = tokens of the batch / device time of one step (CUDA events on the launching stream).
 
-Default workload: LLaMA-3.1-8B full-attention layer, one request of 32768 tokens (32/8 heads,
-d_k 128, hidden 4096, G 64, n 128, A 128, p 0.99), synthetic seeded bf16 inputs.  L2 is
+Default workload: a Gemma-3-12B-shaped full-attention layer under load, 64 requests of 32768 tokens
+packed (2,097,152 tokens; 16/8 heads, d_k 256, hidden 3840, G 64, n 128, A 128, p 0.99), the
+largest workload that fits one GPU, with seeded synthetic bf16 inputs.  The same line carries, under
+"per_config", the other four workloads measured the same way (one 4K and one 32K LLaMA-3.1-8B-shaped
+request, 16 log-uniform requests of 4K-128K, four Qwen3-Next-shaped 128K requests).  L2 is
 flushed (512 MB write) before every timed step.  `--impl reference` times the fp64 CPU oracle
 on the host cores instead (bounded sample of the same workload per step).  `--sweep rho|ablation`
 prints measured sweeps instead of the step line (compaction against the kept fraction; the stages
@@ -41,7 +44,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload index 1..5 (default 2: LLaMA-3.1-8B, 32K)")
+    ap.add_argument("--config", type=int, default=5,
+                    help="workload index 1..5 (default 5: Gemma-3-12B layer geometry, 64 x 32K, the largest)")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the other four workloads' measurement (the 'per_config' object of the line)")
+    ap.add_argument("--per-config-steps", type=int, default=100)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
@@ -117,7 +124,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------------------------------------ our arm
 
-def run_gb300(args, w, rank, world):
+def run_gb300(args, w, rank, world, steps=None, sample_clocks=True):
     import torch
     import long_context_prefill_varlen_gb300 as up
     from synth import cpu as gen
@@ -191,21 +198,22 @@ def run_gb300(args, w, rank, world):
         graph.replay()
     torch.cuda.synchronize()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(dev.index) if rank == 0 else None
+    steps = args.steps if steps is None else steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sampler = ClockSampler(dev.index) if rank == 0 and sample_clocks else None
     time.sleep(0.3 if sampler else 0)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    for k in range(args.steps):
+    for k in range(steps):
         flush.fill_(1)                      # L2 flush, outside the event pair
         ev[k][0].record(stream)
         graph.replay()
         ev[k][1].record(stream)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
-    launches = per_step * args.steps
+    launches = per_step * steps
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop(t0, t1) if sampler else None
@@ -222,7 +230,7 @@ def run_gb300(args, w, rank, world):
     # Per-stage breakdown (eager launches, an event between stages, L2 flushed before each step): it
     # attributes the step's time; each stage's share includes its own launch gaps.
     nst = 7
-    nb = min(args.steps, 100)
+    nb = min(steps, 100)
     marks = [[torch.cuda.Event(enable_timing=True) for _ in range(nst)] for _ in range(nb)]
     torch.cuda.synchronize()
     for k in range(nb):
@@ -234,10 +242,31 @@ def run_gb300(args, w, rank, world):
     for k in range(nb):
         for i in range(nst - 1):
             stage_ms[k, i] = marks[k][i].elapsed_time(marks[k][i + 1])
+    del graph
     return dict(ms=ms, spread=spread, eager_ms=float(stage_ms.sum(axis=1).mean()), stage_ms=stage_ms.mean(axis=0),
-                launches=launches, clocks=clocks, kept=kept,
-                kstar=step.kstar.cpu().tolist(), step=step, inputs=inputs, run_step=run_step, dev=dev,
+                launches=launches, per_step_launches=per_step, clocks=clocks, kept=kept,
+                kstar=step.kstar.cpu().tolist(), near_threshold=near_threshold_blocks(w, step), step=step,
+                inputs=inputs, run_step=run_step, dev=dev,
                 flush=flush, geometry=dict(L=L, layer=layer, B=B, table=table, orig_len=orig_len, kv_len=kv_len))
+
+
+def near_threshold_blocks(w, step, rtol=1e-3):
+    """Blocks, other than each request's k*-th ranked block, whose score lies within rtol (relative) of
+    that block's score tau, from the GPU's own block scores: the only blocks whose keep decision the
+    parity tolerance lets differ from the oracle's (the parity tests count the actual differences)."""
+    bs = step.block_scores.cpu().numpy().astype(np.float64)
+    ks = step.kstar.cpu().numpy()
+    cu = w.cu_seqlens()
+    b0, count = 0, 0
+    for r in range(w.R):
+        nb = -(-(cu[r + 1] - cu[r]) // w.G)
+        if nb and ks[r] > 0:
+            b = bs[b0:b0 + nb]
+            order = np.lexsort((-np.arange(nb), -b))         # descending score, then higher index first
+            tau = b[order[ks[r] - 1]]
+            count += int((np.abs(b - tau) <= rtol * tau).sum()) - 1
+        b0 += nb
+    return count
 
 
 def e2e_measure(args, w, ctx):
@@ -584,44 +613,15 @@ def main():
     pk, pk_kind = peaks()
     ms = res["ms"]
     T_all = w.T * world
-    st = res["stage_ms"]
-    names = ["score", "select", "compact", "slot_mapping", "scatter_back", "seqused"]
-    kept = res["kept"]
-    hb = w.hdim * 2
-    flops = score_flops(w)
-    bytes_rows = 2 * kept * hb                                  # read + write of every kept row
-    stages = {}
-    for i, nm in enumerate(names):
-        stages[nm] = {"ms": float(st[i])}
-    sbytes = score_input_bytes(w)
-    stages["score"].update({"tflops": flops / (st[0] * 1e-3) / 1e12,
-                            "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
-                            "frac_of_bf16_peak_one_pass_equiv": flops / 2 / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
-                            "input_gbs": sbytes / (st[0] * 1e-3) / 1e9,
-                            "frac_of_hbm": sbytes / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"]})
-    for nm in ("compact", "scatter_back"):
-        i = names.index(nm)
-        gbs = (bytes_rows + kept * 4) / (st[i] * 1e-3) / 1e9
-        stages[nm].update({"gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]})
-    stages["select"]["us"] = float(st[1] * 1e3)
-    ssc = float(st[0] + st[1] + st[2])
-    # roofline of the dominant kernel: the row copy (up_scatter_back is exactly one launch of it, and the
-    # same kernel does compaction's gather); the score passes are reported per call under "stages"
-    sc_ms = float(st[4])
-    row_bytes = bytes_rows + kept * 4
-    rl = {"bound": "hbm", "kernel": "rows_kernel (up_scatter_back: one launch per step)",
-          "achieved": row_bytes / (sc_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
-          "algorithmic_bytes": row_bytes}
-    rl["frac"] = rl["achieved"] / rl["peak"]
-    rl["traffic"] = measured_traffic("rows_kernel", w)
-    rl["peak_source"] = pk_kind
+    summ = summarize(w, res, pk, pk_kind)
     line = {"metric": METRIC, "value": T_all / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": workload_config(w),
-            "roofline": rl, "gpu_launches": int(res["launches"]), "clocks": res["clocks"],
-            "score_select_compact_tokens_per_s": T_all / (ssc * 1e-3), "kept_tokens": kept,
-            "kstar": res["kstar"][:8], "ms_per_step_spread": res["spread"], "eager_ms_per_step": res["eager_ms"],
-            "stages": stages}
+            "roofline": summ.pop("roofline"), "gpu_launches": int(res["launches"]), "clocks": res["clocks"],
+            "score_select_compact_tokens_per_s": T_all / (summ["score_select_compact_ms"] * 1e-3),
+            "kept_tokens": res["kept"], "kstar": res["kstar"][:8], "ms_per_step_spread": res["spread"],
+            "eager_ms_per_step": res["eager_ms"], "launches_per_step": res["per_step_launches"],
+            "near_threshold_blocks": res["near_threshold"], "stages": summ["stages"]}
     if not args.no_e2e:
         line["e2e"] = e2e_measure(args, w, res)
     if world == 1 and not args.no_cpu_baseline:
@@ -633,7 +633,71 @@ def main():
                                 "sample": (f"the whole workload ({sample} tokens)" if sw[0] is w else
                                            f"one request of {sample} tokens with the workload's geometry")
                                           + ": score+select+compact+scatter in fp64 numpy, inputs excluded"}
+    if world == 1 and not args.no_per_config:
+        # the other workloads, each measured the same way (graph replays, L2 flushed, events on the stream)
+        del res
+        _free_device_memory()
+        per = {}
+        for i in sorted(recipe.CONFIGS):
+            if i == args.config:
+                continue
+            wi = recipe.workload(i)
+            ri = run_gb300(args, wi, rank, world, steps=max(3, args.per_config_steps), sample_clocks=False)
+            si = summarize(wi, ri, pk, pk_kind)
+            per[str(i)] = {"workload": wi.name, "R": wi.R, "T": wi.T, "Hq": wi.Hq, "Hkv": wi.Hkv, "d_k": wi.dk,
+                           "hidden": wi.hdim, "G": wi.G, "n": wi.n, "p": wi.p,
+                           "tokens_per_s": wi.T / (ri["ms"] * 1e-3), "ms_per_step": ri["ms"],
+                           "score_select_compact_tokens_per_s": wi.T / (si["score_select_compact_ms"] * 1e-3),
+                           "rho": ri["kept"] / max(1, wi.T), "kept_tokens": ri["kept"],
+                           "kstar": {"min": int(min(ri["kstar"])), "max": int(max(ri["kstar"])),
+                                     "first": [int(k) for k in ri["kstar"][:4]]},
+                           "near_threshold_blocks": ri["near_threshold"],
+                           "launches_per_step": ri["per_step_launches"], "steps": max(3, args.per_config_steps),
+                           "roofline": si["roofline"], "stages": si["stages"]}
+            del ri
+            _free_device_memory()
+        line["per_config"] = per
     print(json.dumps(line), flush=True)
+
+
+def _free_device_memory():
+    import gc
+    import torch
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def summarize(w, res, pk, pk_kind):
+    """Stage times and roofline fractions of one measured workload (eager breakdown of run_gb300)."""
+    st = res["stage_ms"]
+    names = ["score", "select", "compact", "slot_mapping", "scatter_back", "seqused"]
+    kept = res["kept"]
+    flops = score_flops(w)
+    bytes_rows = 2 * kept * w.hdim * 2                           # read + write of every kept row
+    stages = {nm: {"ms": float(st[i])} for i, nm in enumerate(names)}
+    sbytes = score_input_bytes(w)
+    stages["score"].update({"tflops": flops / (st[0] * 1e-3) / 1e12,
+                            "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
+                            "frac_of_bf16_peak_one_pass_equiv": flops / 2 / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
+                            "input_gbs": sbytes / (st[0] * 1e-3) / 1e9,
+                            "frac_of_hbm": sbytes / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"]})
+    for nm in ("compact", "scatter_back"):
+        i = names.index(nm)
+        gbs = (bytes_rows + kept * 4) / (st[i] * 1e-3) / 1e9
+        stages[nm].update({"gbs": gbs, "frac_of_hbm": gbs / pk["hbm_gbs"]})
+    stages["select"]["us"] = float(st[1] * 1e3)
+    # roofline of the dominant kernel: the row copy (up_scatter_back is exactly one launch of it, and the
+    # same copy does compaction's gather); the score call is reported under "stages"
+    sc_ms = float(st[4])
+    row_bytes = bytes_rows + kept * 4
+    rl = {"bound": "hbm", "kernel": "rows_kernel (up_scatter_back: one launch per step)",
+          "achieved": row_bytes / (sc_ms * 1e-3) / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+          "algorithmic_bytes": row_bytes}
+    rl["frac"] = rl["achieved"] / rl["peak"]
+    rl["traffic"] = measured_traffic("rows_kernel", w)
+    rl["peak_source"] = pk_kind
+    return {"stages": stages, "roofline": rl, "score_select_compact_ms": float(st[0] + st[1] + st[2])}
 
 
 if __name__ == "__main__":

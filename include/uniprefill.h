@@ -124,8 +124,9 @@ up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const int32_t* c
  *   token_keep_i = [block(i) among the first k*] or i < A (sinks) or i >= N - n (window);
  *   block_keep_g = any token of B_g kept.
  * block_scores: fp32 [nb_cap], finite and >= 0.  p in (0, 1]; A >= 0; n >= 1; G a power of two.
- * block_keep: u8 [nb_cap]; token_keep: u8 [T] (may be NULL when T = 0); kstar: int32 [R] (0 for
- * empty requests).
+ * block_keep: u8 [nb_cap]; token_keep: u8 [T], 16-byte aligned (it is written with 16-byte stores;
+ * a misaligned pointer returns UP_ERR_SHAPE; may be NULL when T = 0); kstar: int32 [R] (0 for empty
+ * requests).
  * At most UP_MAX_BLOCKS_PER_REQUEST blocks per request (else UP_DEV_TOO_MANY_BLOCKS). */
 up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,
                          const int32_t* cu_seqlens, int R, int64_t T, int64_t nb_cap,
@@ -166,7 +167,9 @@ up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seqlens, int R
  * GPU that loads the library until the process exits; the call allocates nothing.
  *  - T > UP_NOALLOC_MAX_TOKENS returns UP_ERR_WORKSPACE before any launch (use up_compact instead).
  *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
- *    device current; make that first call before any stream capture.
+ *    device current; make that first call before any stream capture.  The address is kept for the
+ *    rest of the process: after cudaDeviceReset on that device the entry point must not be called
+ *    again (the library's device image, and with it the array, may have moved).
  *  - Every call on a device shares the one array and leaves its contents behind (nothing in it needs
  *    clearing: each call overwrites what it reads).  Calls whose kernels can overlap on the GPU (for
  *    example on two streams without ordering between them) race on it and give wrong results; order

@@ -334,6 +334,7 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || nb_cap < 0 || G <= 0 || n < 1 || A < 0) return UP_ERR_ARG;
     if (!(p > 0.0) || !(p <= 1.0)) return UP_ERR_ARG;
     if (G & (G - 1)) return UP_ERR_SHAPE;          // block size must be a power of two
+    if (T > 0 && !aligned16(token_keep)) return UP_ERR_SHAPE;   // the mask is written 16 bytes per store
     static int attr_done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return UP_ERR_CUDA;

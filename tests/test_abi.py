@@ -70,6 +70,9 @@ def test_host_validation_returns_before_any_launch(lib):
     assert s == up.UP_ERR_ARG                      # p outside (0, 1]
     s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.0, fake, fake, fake, fake, null)
     assert s == up.UP_ERR_ARG
+    odd = ctypes.c_void_p(0x1001)      # a token mask that is not 16-byte aligned (a view at an odd offset)
+    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.99, fake, odd, fake, fake, null)
+    assert s == up.UP_ERR_SHAPE
     s = lib.up_compact(fake, fake, 1, 4096, fake, 12, null, null, fake, null, null, fake, fake, fake, fake, null,
                        null, 0, 0, fake, 1 << 20, fake, null)
     assert s == up.UP_ERR_SHAPE                    # hidden size must be a multiple of 8

@@ -4,8 +4,12 @@ Some callers cannot give this library device scratch memory: an engine whose mem
 device memory once it has started, a plugin host that only hands over the tensors it already holds,
 or a loop that must not pay cudaMalloc's implicit synchronisation.  up_compact_noalloc serves them with
 a fixed scratch array built into the library.  This file checks, through the C ABI, that it returns
-exactly what the workspace version returns (compaction is bit-exact), on two calls in a row so that
-whatever the first call leaves in the shared array cannot leak into the second.  It runs last.
+exactly what the workspace version returns (compaction is bit-exact) and what the fp64 oracle's
+compaction gives, on calls in a row so that whatever one call leaves in the shared array cannot leak
+into the next.  The streams take every launch path of the compaction through the shared array: at
+most 8 tiles of 1,024 tokens (one launch that scans the stream itself), up to 64 tiles (the scan
+kernel counts the tiles) and more than 64 tiles (a separate count kernel writes the tile counts).
+It runs last.
 """
 import ctypes
 
@@ -14,6 +18,7 @@ import pytest
 import torch
 
 import long_context_prefill_varlen_gb300 as up
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -64,13 +69,31 @@ def _run(c, noalloc):
     return res
 
 
-def test_noalloc_matches_the_workspace_version_on_two_calls_in_a_row():
-    cases = [_case(1, 0.7, [5000, 0, 37, 12000, 1025]), _case(2, 0.25, [3000, 9000, 1, 4096])]
+def _against_oracle(c, got):
+    """the noalloc outputs, bit-exact against the oracle's compaction of the same mask and inputs"""
+    n = int(got["num_actual"][0])
+    kl = got["kept_len"].numpy()
+    g = dict(num_actual=n, kept_index=got["kept_index"].numpy(), new_cu=got["new_cu"].numpy(),
+             new_len=got["new_len"].numpy(), out_hidden=got["out_hidden"].numpy().view(np.uint16),
+             out_positions=got["out_pos"].numpy(), out_slots=got["out_slots"].numpy(), kept_len=kl,
+             drop_layer=got["drop_layer"].numpy())
+    parity.check_compaction(g, c["keep"].cpu().numpy(), c["cu"].cpu().numpy(),
+                            hidden=c["hidden"].cpu().view(torch.int16).numpy().view(np.uint16),
+                            positions=c["pos"].cpu().numpy(), slots=c["slots"].cpu().numpy(), layer=1)
+
+
+def test_noalloc_matches_the_workspace_version_and_the_oracle_on_calls_in_a_row():
+    cases = [_case(1, 0.7, [5000, 0, 37, 12000, 1025]),      # 18 tiles: the scan kernel counts the tiles
+             _case(2, 0.25, [3000, 9000, 1, 4096]),          # 16 tiles
+             _case(3, 0.5, [70000, 3, 1200], hdim=64),       # 70 tiles: separate count kernel
+             _case(4, 0.9, [2000, 0, 4100, 1], hdim=64),     # 6 tiles: the one-launch path
+             _case(5, 0.1, [66000, 50], hdim=64)]            # 65 tiles again, after a short stream
     for c in cases:
         ref = _run(c, noalloc=False)
         got = _run(c, noalloc=True)
         for k in ref:
             assert torch.equal(ref[k], got[k]), k
+        _against_oracle(c, got)
 
 
 def test_noalloc_rejects_more_tokens_than_its_scratch_holds():
