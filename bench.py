@@ -567,18 +567,20 @@ def measured_traffic(kernel, w):
 
 
 def score_input_bytes(w):
-    """DRAM input of both passes: K once per pass, plus the window rows of Q once per (KV head) unit."""
+    """DRAM input of the score call: K once, plus the window rows of Q once per (KV head) unit."""
     kb = w.T * w.Hkv * w.dk * 2
     qb = sum(min(w.n, N) for N in w.lengths) * w.Hq * w.dk * 2
-    return 2 * (kb + qb)
+    return kb + qb
 
 
 def score_flops(w):
-    """Algorithmic FLOPs of both passes: 2 * d_k * (n_eff*N - n_eff(n_eff-1)/2) per (request, query head, pass)."""
+    """Algorithmic FLOPs of the score call: S = Q K^T over the causal support once,
+    2 * d_k * (n_eff*N - n_eff(n_eff-1)/2) per (request, query head).  The call computes S once (the
+    one-pass form; a second pass over the block sums replaces the recompute of S)."""
     tot = 0
     for N in w.lengths:
         ne = min(w.n, N)
-        tot += 2 * w.dk * (ne * N - ne * (ne - 1) // 2) * w.Hq * 2
+        tot += 2 * w.dk * (ne * N - ne * (ne - 1) // 2) * w.Hq
     return tot
 
 
@@ -679,7 +681,6 @@ def summarize(w, res, pk, pk_kind):
     sbytes = score_input_bytes(w)
     stages["score"].update({"tflops": flops / (st[0] * 1e-3) / 1e12,
                             "frac_of_bf16_peak": flops / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
-                            "frac_of_bf16_peak_one_pass_equiv": flops / 2 / (st[0] * 1e-3) / 1e12 / pk["bf16_tflops"],
                             "input_gbs": sbytes / (st[0] * 1e-3) / 1e9,
                             "frac_of_hbm": sbytes / (st[0] * 1e-3) / 1e9 / pk["hbm_gbs"]})
     for nm in ("compact", "scatter_back"):

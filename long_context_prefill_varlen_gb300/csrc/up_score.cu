@@ -60,7 +60,7 @@ struct Geometry {
 };
 
 struct Layout {
-    size_t items, unit_items, n_items, ml, cvec, blk, tok, total;
+    size_t items, unit_items, n_items, ml, cvec, blk, tok, be, bm, total;
     int64_t items_cap, units;
 };
 
@@ -79,6 +79,9 @@ struct Params {
     float* cvec;
     float* blk;
     float* tok;
+    float* be;             // one pass: per (unit, key tile, block of the tile, row) block sums of 2^(S*a - m_t)
+    float* bm;             // one pass: per (unit, key tile, row) the reference m_t of those sums
+    int spt;               // one pass: blocks per key tile (128 / G)
     float* block_scores;
     float* token_scores;
     int32_t* status;
@@ -97,11 +100,17 @@ struct JobMap {
     int J, W, nbuf, nb_log, wpj;
 };
 __host__ __device__ constexpr int wg_per_job(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
+// PASS 3 is the one-pass form of pass 1 (see epilogue_one_pass): the jobs of pass 1, each TMEM buffer
+// drained whole by one warpgroup.
 template <int PASS>
 __host__ __device__ __forceinline__ JobMap job_map(const Params& P) {
     if (PASS == 2 && P.wide2) return JobMap{P.J / 2, 256, 2, 1, 4};
+    if (PASS == 3) return JobMap{P.J, 128, 4, 2, 1};
     return JobMap{P.J, 128, 4, 2, wg_per_job(P.J)};
 }
+
+// The one pass applies to slabs of 1, 2 or 4 jobs (a warpgroup then always drains the same job).
+__host__ __device__ constexpr bool one_pass_ok(int J) { return J == 1 || J == 2 || J == 4; }
 
 static bool geometry(int Hq, int Hkv, int dk, int n, Geometry* g) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
@@ -129,7 +138,7 @@ static int work_sets(int units_per_req, int slabs, int sms) {
     return 1;
 }
 
-static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_cap, bool tok) {
+static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_cap, bool tok, int G) {
     Layout L{};
     L.items_cap = (cdiv(T, (int64_t)kTileKeys * kItemTiles) + R) * Hkv * g.slabs;
     L.units = (int64_t)R * Hkv * g.slabs;
@@ -142,6 +151,13 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
     L.cvec = take(sizeof(float) * L.units * g.slab_rows);
     L.blk = take(sizeof(float) * (size_t)Hkv * g.slabs * 4 * nb_cap);      // one partial per warpgroup
     L.tok = tok ? take(sizeof(float) * (size_t)Hkv * g.slabs * 4 * T) : 0;
+    if (one_pass_ok(g.J)) {
+        // block sums and their reference maxima of the one pass, per (unit, key tile, row); a unit's tiles
+        // start at twice its first item's index in the plan's dense per-unit item numbering
+        const size_t tiles = static_cast<size_t>(L.items_cap) * kItemTiles;
+        L.be = take(sizeof(float) * tiles * (kTileKeys / G) * g.slab_rows);
+        L.bm = take(sizeof(float) * tiles * g.slab_rows);
+    }
     L.total = o;
     return L;
 }
@@ -455,8 +471,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                         const uint64_t qdc = desc_add(qd, c * slab_chunk_bytes);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
-                            const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
+                            const uint64_t a = PASS != 2 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
+                            const uint64_t b = PASS != 2 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
                             if (leader) tc_mma_bf16(d_tmem, a, b, idesc, (c | k) != 0);
                         }
                     }
@@ -491,8 +507,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                         const uint64_t qdc = desc_add(slab_d0, j * jm.W * 128 + c * slab_chunk_bytes);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint64_t a = PASS == 1 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
-                            const uint64_t b = PASS == 1 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
+                            const uint64_t a = PASS != 2 ? desc_add(qdc, k * 32) : desc_add(kd, k * 32);
+                            const uint64_t b = PASS != 2 ? desc_add(kd, k * 32) : desc_add(qdc, k * 32);
                             if (leader) tc_mma_bf16(d_tmem, a, b, idesc, (c | k) != 0);
                         }
                     }
@@ -894,6 +910,164 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
     }
 }
 
+// ------------------------------------------------------------------------------------------------
+// the one pass: row statistics and block sums from a single Q.K^T
+//
+// Per window row j and key tile t, the thread that owns row j (rows are TMEM lanes) computes with its
+// running maximum m_t (base 2, over the keys it has seen up to the end of tile t) the sums
+//   e_{j,g} = sum_{i in B_g} 2^(S_ji * a - m_t)      for the 128 / G blocks g of tile t,
+// and writes them with m_t.  The usual (m, l) partials per work item are written as in pass 1, so the
+// merge kernel gives c_j = m_j + log2(l_j), and the reduce kernel then forms Eq. 4 exactly:
+//   sum_j sum_{i in B_g} A_ji = sum_j e_{j,g} * 2^(m_t - c_j).
+// This is the two-pass softmax of the section 3.5 kernel design with the second pass run over the block
+// sums (G times smaller than S) instead of over a recomputed S: the tensor work and the exponentials of
+// the recompute pass disappear; S itself is never stored.
+
+// one 16-column chunk of this thread's row in the one pass: fold its maximum into m (rescaling the block
+// sums of the tile so far and the l of the item's earlier tiles when it grows), then add the sum of
+// 2^(S*a - m) over the chunk to its block's sum e[ch / CPB] (CPB = G / 16 chunks per block).  Columns
+// outside the causal range arrive as -inf and add 0.
+template <int CPB>
+__device__ __forceinline__ void one_pass_chunk(const uint32_t (&v)[16], int ch, float a, float& m, float& l,
+                                               float (&e)[8 / CPB]) {
+    const float x0 = max3(f(v[0]), f(v[1]), f(v[2])), x1 = max3(f(v[3]), f(v[4]), f(v[5]));
+    const float x2 = max3(f(v[6]), f(v[7]), f(v[8])), x3 = max3(f(v[9]), f(v[10]), f(v[11]));
+    const float x4 = max3(f(v[12]), f(v[13]), f(v[14]));
+    const float mx = max3(max3(x0, x1, x2), max3(x3, x4, f(v[15])), x0) * a;
+    if (mx > m) {
+        const float sc = ex2(m - mx);           // 0 while m = -inf
+        l *= sc;
+#pragma unroll
+        for (int b = 0; b < 8 / CPB; ++b)
+            if (b <= ch / CPB) e[b] *= sc;
+        m = mx;
+    }
+    // while m is -inf every value so far is -inf: any finite reference gives the sum 0, not NaN
+    const float mr = m == -INFINITY ? 0.f : m;
+    const uint64_t a2 = pk2(a, a), nm2 = pk2(-mr, -mr);
+    uint64_t s0 = p2(v, 0, a2, nm2), s1 = p2(v, 2, a2, nm2);
+#pragma unroll
+    for (int c = 4; c < 16; c += 4) {
+        s0 = add2(s0, p2(v, c, a2, nm2));
+        s1 = add2(s1, p2(v, c + 2, a2, nm2));
+    }
+    const float2 t = up2(add2(s0, s1));
+    e[ch / CPB] += t.x + t.y;
+}
+
+// columns 16*ch + c > lim of a chunk become -inf (keys after the row's position, or a row that is not a
+// window row of this request: lim < 0)
+__device__ __forceinline__ void mask_chunk(uint32_t (&v)[16], int ch, int lim) {
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+        if (16 * ch + c > lim) v[c] = 0xFF800000u;
+}
+
+// one whole 128-column job of this thread's row: eight chunks, TMEM loads double-buffered, the buffer
+// released as soon as its last chunk has landed; `masked` (warp-uniform) applies the causal limit lim
+template <int CPB>
+__device__ __forceinline__ void one_pass_tile(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool masked, int lim,
+                                              float a, float& m, float& l, float (&e)[8 / CPB]) {
+    uint32_t va[16], vb[16];
+    tmem_ld16(ta, va);
+    tmem_wait_pin(va);
+#pragma unroll
+    for (int ch = 0; ch < 8; ch += 2) {
+        tmem_ld16(ta + (ch + 1) * 16, vb);
+        if (masked) mask_chunk(va, ch, lim);
+        one_pass_chunk<CPB>(va, ch, a, m, l, e);
+        tmem_wait_pin(vb);
+        if (ch + 2 < 8) tmem_ld16(ta + (ch + 2) * 16, va);
+        else release_tmem(S, buf, lane);
+        if (masked) mask_chunk(vb, ch + 1, lim);
+        one_pass_chunk<CPB>(vb, ch + 1, a, m, l, e);
+        if (ch + 2 < 8) tmem_wait_pin(va);
+    }
+}
+
+// Warpgroup w drains TMEM buffer w: with J in {1, 2, 4} jobs per tile that is always job w % J (the
+// same 128 window rows), on every (4 / J)-th tile of the CTA's sequence.  The warpgroups that hold the
+// same rows merge their (m, l) at the end of each item in a fixed order, as in pass 1.  CPB = G / 16.
+template <int CPB>
+__device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
+    constexpr int SPT = 8 / CPB;                // blocks per tile
+    volatile int* abort_flag = S.abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = (warp - 2) >> 2;             // warpgroup 0..3 = the TMEM buffer it drains
+    const int q = warp & 3;                     // TMEM lane quarter this warp may access
+    const int rl = q * 32 + lane;
+    const int J = P.J;
+    const int j = wg % J;                       // the job (128 rows of the slab) of this warpgroup
+    const int row = j * 128 + rl;               // this thread's row in the slab
+    const float a = P.a;
+    const uint32_t ta = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + wg * 128;
+    uint32_t tiles_done = 0;
+    int prev_slab = -1;
+    bool rin = false;
+    int rmod = 0;
+    for (int it = it0; it < it1; ++it) {
+        const ItemInfo I = item_info(P, it);
+        if (I.slab != prev_slab) {
+            const int qg = I.slab * P.slab_rows + row;
+            rin = qg < P.rows_total;
+            rmod = qg % P.n;
+            prev_slab = I.slab;
+        }
+        const int pos = I.N - P.n + rmod;       // this row's position in the request
+        const bool rvalid = rin && pos >= 0;
+        const int2 ui = P.unit_items[I.unit];
+        const size_t tile0 = static_cast<size_t>(ui.x) * kItemTiles;   // the unit's first key tile
+        float m = -INFINITY, l = 0.f;
+        for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
+            const uint32_t jc = tiles_done * J + j;
+            if ((jc & 3u) != static_cast<uint32_t>(wg)) continue;           // another warpgroup's tile
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + wg), (jc >> 2) & 1, abort_flag));
+            tc_fence_after();
+            if (!ok) {
+                release_tmem(S, wg, lane);
+                continue;
+            }
+            const int lim = rvalid ? pos - kt * kTileKeys : -1;               // last visible column
+            float e[SPT];
+#pragma unroll
+            for (int b = 0; b < SPT; ++b) e[b] = 0.f;
+            const bool masked = !__all_sync(0xffffffffu, lim >= kTileKeys - 1);
+            one_pass_tile<CPB>(S, ta, wg, lane, masked, lim, a, m, l, e);
+            const size_t t = tile0 + kt;
+            P.bm[t * P.slab_rows + row] = m;
+            float* dst = P.be + t * SPT * P.slab_rows + row;
+            float ts = 0.f;
+#pragma unroll
+            for (int b = 0; b < SPT; ++b) {
+                dst[static_cast<size_t>(b) * P.slab_rows] = e[b];
+                ts += e[b];
+            }
+            l += ts;
+        }
+        // this item's (m, l) partial of the row, merged over the 4 / J warpgroups that hold the row
+        float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;
+        if (J == 4) {
+            part[(size_t)row * ui.y] = make_float2(m, l);
+        } else {
+            float2* xm = reinterpret_cast<float2*>(S.xchg);                  // [4 warpgroups][128 rows]
+            xm[wg * 128 + rl] = make_float2(m, l);
+            named_bar_sync(1, kEpiThreads);
+            if (wg < J) {
+                float mm = -INFINITY;
+                for (int w2 = wg; w2 < 4; w2 += J) mm = fmaxf(mm, xm[w2 * 128 + rl].x);
+                float ll = 0.f;
+                if (mm > -INFINITY)
+                    for (int w2 = wg; w2 < 4; w2 += J) {
+                        const float2 x = xm[w2 * 128 + rl];
+                        ll += x.y * ex2(x.x - mm);
+                    }
+                part[(size_t)row * ui.y] = make_float2(mm, ll);
+            }
+            named_bar_sync(1, kEpiThreads);
+        }
+    }
+}
+
 // Fold each query row's pass-1 partials (one per work item of its unit, in the unit's key-tile order)
 // into c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
 __global__ void __launch_bounds__(256) merge_kernel(Params P) {
@@ -980,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // predecessor (the plan kernel) writes, so every warp waits here.  Pass 2's producer and MMA warps
     // read only Q, K and the items, complete since before pass 1 ran, so they start at once; only its
     // epilogue waits, for the row normalisers of its predecessor (the merge kernel).
-    if (PASS == 1) pdl_wait();
+    if (PASS != 2) pdl_wait();
     pdl_trigger();
     const int n_items = uni(__ldcg(P.n_items));
     int it0, it1;
@@ -996,6 +1170,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         producer<NC>(P, S, &tmQ, &tmK, it0, it1);
     } else if (warp == 1 || warp == kIssuer1Warp) {
         mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : 1u);
+    } else if (PASS == 3) {
+        switch (P.spt) {                         // blocks per key tile = 128 / G
+            case 8: epilogue_one_pass<1>(P, S, tmem_base, it0, it1); break;
+            case 4: epilogue_one_pass<2>(P, S, tmem_base, it0, it1); break;
+            case 2: epilogue_one_pass<4>(P, S, tmem_base, it0, it1); break;
+            default: epilogue_one_pass<8>(P, S, tmem_base, it0, it1); break;
+        }
     } else {
         const JobMap jm = job_map<PASS>(P);
         switch (jm.W / 16 / jm.wpj) {            // 16-column chunks per job slice
@@ -1063,6 +1244,92 @@ __global__ void finalize_kernel(Params P) {
     }
 }
 
+// The one pass's Eq. 4: one CTA per (request, key tile) forms the tile's SPT = 128 / G block scores
+//   b_g = 1/(n_eff * Hq * G) * sum over the request's units and their rows j of e_{j,g} * 2^(m_t,j - c_j).
+// Threads take (unit, group of 4 rows) pairs in a fixed assignment, with 16-byte loads, several pairs'
+// loads in flight before any is used; per-thread sums are reduced by warp shuffles and then over the
+// warps in warp order.  Deterministic.
+constexpr int kReduceThreads = 256;
+constexpr int kMaxUnitsPerReq = 1024;
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+template <int SPT>
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
+    if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
+    constexpr int B = SPT <= 2 ? 4 : SPT == 4 ? 2 : 1;       // (unit, row group) pairs per thread in flight
+    __shared__ float s_part[kReduceThreads / 32][SPT];
+    __shared__ int s_tile0[kMaxUnitsPerReq];
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int upr = P.units_per_req, rows = P.slab_rows, rows4 = rows / 4;
+    const int pairs = upr * rows4;
+    const int req_items = __ldcg(P.n_items) / upr;          // items of unit 0 of every request
+    for (int task = blockIdx.x; task < req_items * kItemTiles; task += gridDim.x) {
+        // the request: the largest r whose first item (unit_items[r * upr].x / upr) is <= task / 2
+        const int ri = task / kItemTiles;
+        int lo = 0, hi = P.R;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (P.unit_items[mid * upr].x / upr <= ri) lo = mid; else hi = mid;
+        }
+        const int r = lo;
+        const int N = P.cu[r + 1] - P.cu[r];
+        const int tile = task - (P.unit_items[r * upr].x / upr) * kItemTiles;
+        if (N == 0 || tile * kTileKeys >= N) continue;     // the odd tile of a request's last item
+        for (int kk = threadIdx.x; kk < upr; kk += kReduceThreads)
+            s_tile0[kk] = P.unit_items[r * upr + kk].x * kItemTiles + tile;
+        __syncthreads();
+        float acc[SPT];
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
+        for (int i0 = threadIdx.x; i0 < pairs; i0 += B * kReduceThreads) {
+            float4 wv[B], ev[B][SPT];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = i0 + b * kReduceThreads;
+                if (i < pairs) {
+                    const int kk = i / rows4, r0 = (i - kk * rows4) * 4;
+                    const size_t t = static_cast<size_t>(s_tile0[kk]);
+                    const float4 m4 = ldcg4(P.bm + t * rows + r0);
+                    const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
+#pragma unroll
+                    for (int s = 0; s < SPT; ++s) ev[b][s] = ldcg4(P.be + (t * SPT + s) * rows + r0);
+                    wv[b] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
+                } else {
+                    wv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int s = 0; s < SPT; ++s) ev[b][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int s = 0; s < SPT; ++s)
+                    acc[s] += (ev[b][s].x * wv[b].x + ev[b][s].y * wv[b].y) + (ev[b][s].z * wv[b].z + ev[b][s].w * wv[b].w);
+        }
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            float x = acc[s];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) s_part[w][s] = x;
+        }
+        __syncthreads();
+        if (threadIdx.x < SPT) {
+            const int g = tile * SPT + threadIdx.x;
+            if (g * P.G < N) {
+                float x = 0.f;
+                for (int w2 = 0; w2 < kReduceThreads / 32; ++w2) x += s_part[w2][threadIdx.x];
+                const int ne = min(P.n, N);
+                P.block_scores[P.cb[r] + g] = x * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
+            }
+        }
+        __syncthreads();
+    }
+}
+
 // ------------------------------------------------------------------------------------------------
 // host
 
@@ -1112,16 +1379,41 @@ static cudaError_t launch_pass(const CUtensorMap& q, const CUtensorMap& k, const
     return e;
 }
 
+static cudaError_t launch_merge(const Params& P, int64_t merge_rows, cudaStream_t st) {
+    const int mgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(merge_rows, 8), 16 * num_sms())));
+    const cudaError_t e = launch_pdl(merge_kernel, dim3(mgrid), dim3(256), 0, st, P);
+    count_launch();
+    return e;
+}
+
+// two passes (row statistics, merge, recompute with the column sums); finalize follows
 template <int NC>
 static cudaError_t launch_both(const CUtensorMap& q, const CUtensorMap& k, const Params& P, int grid,
                                int64_t merge_rows, cudaStream_t st) {
     cudaError_t e = launch_pass<1, NC>(q, k, P, grid, st);
     if (e != cudaSuccess) return e;
-    const int mgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(merge_rows, 8), 16 * num_sms())));
-    e = launch_pdl(merge_kernel, dim3(mgrid), dim3(256), 0, st, P);
-    count_launch();
+    e = launch_merge(P, merge_rows, st);
     if (e != cudaSuccess) return e;
     return launch_pass<2, NC>(q, k, P, grid, st);
+}
+
+// one pass (row statistics and block sums), merge, reduce into the block scores
+template <int NC>
+static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const Params& P, int grid,
+                              int64_t merge_rows, int64_t req_tiles, cudaStream_t st) {
+    cudaError_t e = launch_pass<3, NC>(q, k, P, grid, st);
+    if (e != cudaSuccess) return e;
+    e = launch_merge(P, merge_rows, st);
+    if (e != cudaSuccess) return e;
+    const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(req_tiles, 8 * num_sms())));
+    switch (P.spt) {
+        case 8: e = launch_pdl(reduce_kernel<8>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 4: e = launch_pdl(reduce_kernel<4>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 2: e = launch_pdl(reduce_kernel<2>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        default: e = launch_pdl(reduce_kernel<1>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+    }
+    count_launch();
+    return e;
 }
 
 }  // namespace score
@@ -1139,8 +1431,8 @@ extern "C" size_t up_score_workspace_bytes(int R, int64_t T, int Hq, int Hkv, in
                                            int with_token_scores) {
     Geometry g;
     if (R <= 0 || T < 0 || T >= (int64_t(1) << 31) || nb_cap < 0 || !geometry(Hq, Hkv, dk, n, &g)) return 0;
-    (void)G;
-    return layout(R, T, g, Hkv, nb_cap, with_token_scores != 0).total;
+    if (G != 16 && G != 32 && G != 64 && G != 128) return 0;
+    return layout(R, T, g, Hkv, nb_cap, with_token_scores != 0, G).total;
 }
 
 extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const int32_t* cu_seqlens, int R,
@@ -1156,7 +1448,9 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     if (!geometry(Hq, Hkv, dk, n, &g)) return UP_ERR_SHAPE;
     if (G != 16 && G != 32 && G != 64 && G != 128) return UP_ERR_SHAPE;
     if (!aligned16(Q) || !aligned16(K) || !aligned16(ws)) return UP_ERR_SHAPE;
-    const Layout L = layout(R, T, g, Hkv, nb_cap, token_scores != nullptr);
+    const Layout L = layout(R, T, g, Hkv, nb_cap, token_scores != nullptr, G);
+    // one tcgen05 pass unless per-token scores are asked for (they need the recompute pass)
+    const bool one_pass = token_scores == nullptr && one_pass_ok(g.J) && Hkv * g.slabs <= kMaxUnitsPerReq;
     if (ws_bytes < L.total) return UP_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
 
@@ -1188,6 +1482,9 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.cvec = reinterpret_cast<float*>(w + L.cvec);
     P.blk = reinterpret_cast<float*>(w + L.blk);
     P.tok = token_scores ? reinterpret_cast<float*>(w + L.tok) : nullptr;
+    P.be = one_pass ? reinterpret_cast<float*>(w + L.be) : nullptr;
+    P.bm = one_pass ? reinterpret_cast<float*>(w + L.bm) : nullptr;
+    P.spt = kTileKeys / G;
     P.block_scores = block_scores;
     P.token_scores = token_scores;
     P.status = dev_status;
@@ -1203,6 +1500,15 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
         grid = grid / P.nsets * P.nsets;
         cudaError_t e;
         const int64_t merge_rows = L.units * g.slab_rows;
+        if (one_pass) {
+            const int64_t req_tiles = L.items_cap / P.units_per_req * kItemTiles;
+            switch (g.nc) {
+                case 1: e = launch_one<1>(tq, tk, P, grid, merge_rows, req_tiles, st); break;
+                case 2: e = launch_one<2>(tq, tk, P, grid, merge_rows, req_tiles, st); break;
+                default: e = launch_one<4>(tq, tk, P, grid, merge_rows, req_tiles, st); break;
+            }
+            return e == cudaSuccess ? UP_OK : UP_ERR_CUDA;
+        }
         switch (g.nc) {
             case 1: e = launch_both<1>(tq, tk, P, grid, merge_rows, st); break;
             case 2: e = launch_both<2>(tq, tk, P, grid, merge_rows, st); break;

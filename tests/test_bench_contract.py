@@ -30,8 +30,8 @@ def test_score_accounting_helpers():
     import bench
     from synth import recipe
     w = recipe.workload(2)
-    # two passes of 2 d_k (n N - n(n-1)/2) per query head, one 32K request, n = 128
+    # S computed once: 2 d_k (n N - n(n-1)/2) per query head, one 32K request, n = 128
     n, N = 128, 32768
-    assert bench.score_flops(w) == 2 * 2 * 128 * (n * N - n * (n - 1) // 2) * 32
-    # K once per pass plus the window rows of Q, both passes
-    assert bench.score_input_bytes(w) == 2 * (N * 8 * 128 * 2 + n * 32 * 128 * 2)
+    assert bench.score_flops(w) == 2 * 128 * (n * N - n * (n - 1) // 2) * 32
+    # K once plus the window rows of Q
+    assert bench.score_input_bytes(w) == N * 8 * 128 * 2 + n * 32 * 128 * 2

@@ -205,42 +205,57 @@ def _run_score(w, host, with_tokens=True):
     return step, d
 
 
+# with per-token scores the call runs the two tcgen05 passes (row statistics, then recompute); without
+# them, one pass that also writes per-row block sums, reduced after the row merge (slabs of 1, 2 or 4
+# jobs of 128 rows; the other shapes keep two passes)
+@pytest.mark.parametrize("tokens", [True, False], ids=["two_pass", "one_pass"])
 @pytest.mark.parametrize("case", SCORE_CASES, ids=lambda c: "Hq%d_Hkv%d_dk%d_G%d_n%d" % c[:5])
-def test_score_matches_oracle(case):
+def test_score_matches_oracle(case, tokens):
     Hq, Hkv, dk, G, n, lengths = case
     w = recipe.small(lengths=lengths, Hq=Hq, Hkv=Hkv, dk=dk, hdim=64, G=G, n=n, salt=50 + dk + G + n)
     host = gen.materialize(w, with_hidden=False)
-    step, _ = _run_score(w, host)
+    step, _ = _run_score(w, host, with_tokens=tokens)
     Q = gen.bf16_bits_to_f32(host["Q"]).astype(np.float64)
     K = gen.bf16_bits_to_f32(host["K"]).astype(np.float64)
     s_ref = oracle.token_scores(Q, K, host["cu_seqlens"], n)
     b_ref = oracle.block_scores_from_tokens(s_ref, host["cu_seqlens"], G)
     nbt = len(b_ref)
     parity.check_block_scores(step.block_scores.cpu().numpy()[:nbt], b_ref)
-    parity.check_block_scores(step.token_scores.cpu().numpy(), s_ref)
+    if tokens:
+        parity.check_block_scores(step.token_scores.cpu().numpy(), s_ref)
 
 
-def test_score_closed_form_at_q_zero():
-    """Q = 0: the scores follow the closed form 1/(n_eff) sum 1/(j+1) whatever K is."""
-    w = recipe.small(lengths=(600, 77), Hq=4, Hkv=2, dk=128, hdim=64, G=64, n=128, salt=5)
+@pytest.mark.parametrize("tokens", [True, False], ids=["two_pass", "one_pass"])
+def test_score_closed_form_at_q_zero(tokens):
+    """Q = 0: the scores follow the closed form 1/(n_eff) sum 1/(j+1) whatever K is (block scores: the
+    closed form summed over the block and divided by G)."""
+    G = 64
+    w = recipe.small(lengths=(600, 77), Hq=4, Hkv=2, dk=128, hdim=64, G=G, n=128, salt=5)
     host = gen.materialize(w, with_hidden=False)
     host["Q"][:] = 0
-    step, _ = _run_score(w, host)
-    s = step.token_scores.cpu().numpy()
+    step, _ = _run_score(w, host, with_tokens=tokens)
+    s = step.token_scores.cpu().numpy() if tokens else None
+    b = step.block_scores.cpu().numpy()
     cu = host["cu_seqlens"]
+    cb = oracle.cu_blocks_of(cu, G)
     for r in range(2):
         N = cu[r + 1] - cu[r]
         ne = min(128, N)
-        for i in range(N):
-            exact = sum(1.0 / (j + 1) for j in range(max(i, N - ne), N)) / ne
-            assert abs(s[cu[r] + i] - exact) <= 1e-4 * exact
+        exact = [sum(1.0 / (j + 1) for j in range(max(i, N - ne), N)) / ne for i in range(N)]
+        if tokens:
+            for i in range(N):
+                assert abs(s[cu[r] + i] - exact[i]) <= 1e-4 * exact[i]
+        for g in range(cb[r + 1] - cb[r]):
+            eb = sum(exact[g * G:(g + 1) * G]) / G
+            assert abs(b[cb[r] + g] - eb) <= 1e-4 * eb
 
 
-def test_score_is_deterministic_and_packing_invariant():
+@pytest.mark.parametrize("tokens", [True, False], ids=["two_pass", "one_pass"])
+def test_score_is_deterministic_and_packing_invariant(tokens):
     w = recipe.small(lengths=(1500, 700, 2100), Hq=8, Hkv=2, dk=128, hdim=64, salt=61)
     host = gen.materialize(w, with_hidden=False)
-    a, _ = _run_score(w, host)
-    b, _ = _run_score(w, host)
+    a, _ = _run_score(w, host, with_tokens=tokens)
+    b, _ = _run_score(w, host, with_tokens=tokens)
     ba, bb = a.block_scores.cpu().numpy(), b.block_scores.cpu().numpy()
     assert np.array_equal(ba, bb)
     cu = host["cu_seqlens"]
@@ -251,7 +266,7 @@ def test_score_is_deterministic_and_packing_invariant():
         hr["cu_seqlens"] = np.array([0, w.lengths[r]], dtype=np.int32)
         hr["Q"] = host["Q"][cu[r]:cu[r + 1]]
         hr["K"] = host["K"][cu[r]:cu[r + 1]]
-        sr, _ = _run_score(wr, hr)
+        sr, _ = _run_score(wr, hr, with_tokens=tokens)
         assert np.array_equal(sr.block_scores.cpu().numpy()[:cb[r + 1] - cb[r]], ba[cb[r]:cb[r + 1]]), r
 
 
