@@ -61,12 +61,13 @@ typedef enum {
 #define UP_DEV_OK               0
 #define UP_DEV_BAD_CU_SEQLENS   1   /* cu_seqlens not 0..T non-decreasing                         */
 #define UP_DEV_BAD_CU_BLOCKS    2   /* cu_blocks inconsistent with cu_seqlens and G, or > nb_cap  */
-#define UP_DEV_TOO_MANY_BLOCKS  3   /* a request has more than UP_MAX_BLOCKS_PER_REQUEST blocks   */
+#define UP_DEV_TOO_MANY_BLOCKS  3   /* a request over UP_MAX_BLOCKS_PER_REQUEST blocks, no select ws */
 #define UP_DEV_WAIT_TIMEOUT     4   /* a pipeline wait inside a kernel ran past its time bound    */
 #define UP_DEV_BAD_POSITION     5   /* Eq. 16: a position beyond its block-table row (slot = -1) */
 #define UP_DEV_BAD_TOKEN_COUNT  6   /* num_actual_tokens outside [0, T_upper]                     */
 
-#define UP_MAX_BLOCKS_PER_REQUEST 8192   /* up_select_topp sorts one request in shared memory */
+#define UP_MAX_BLOCKS_PER_REQUEST 8192   /* up to this many blocks up_select_topp sorts a request in
+                                            shared memory; longer requests need its workspace */
 
 /* ------------------------------------------------------------------------------------------- */
 /* sizing helpers (host only, no CUDA call)                                                     */
@@ -83,7 +84,11 @@ size_t up_score_workspace_bytes(int R, int64_t T, int Hq, int Hkv, int dk, int G
 /* Workspace of up_compact. */
 size_t up_compact_workspace_bytes(int R, int64_t T);
 
-/* One workspace big enough for every call of a drop step (score with token scores, compact). */
+/* Workspace of up_select_topp for block arrays of nb_cap entries (two key arrays of nb_cap uint64). */
+size_t up_select_workspace_bytes(int64_t nb_cap);
+
+/* One workspace big enough for every call of a drop step (score with token scores, select, compact),
+ * which run one after another on a stream and may therefore share it. */
 size_t up_workspace_bytes(int R, int64_t T, int Hq, int Hkv, int dk, int G, int n, int64_t nb_cap);
 
 /* ------------------------------------------------------------------------------------------- */
@@ -127,12 +132,16 @@ up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const int32_t* c
  * block_keep: u8 [nb_cap]; token_keep: u8 [T], 16-byte aligned (it is written with 16-byte stores;
  * a misaligned pointer returns UP_ERR_SHAPE; may be NULL when T = 0); kstar: int32 [R] (0 for empty
  * requests).
- * At most UP_MAX_BLOCKS_PER_REQUEST blocks per request (else UP_DEV_TOO_MANY_BLOCKS). */
+ * ws: device workspace of up_select_workspace_bytes(nb_cap) bytes, 16-byte aligned, no initialisation
+ * needed, or NULL.  A request of at most UP_MAX_BLOCKS_PER_REQUEST blocks is sorted in shared memory and
+ * never touches it; a longer request sorts its keys through it (the same stable passes in tiles of 8192
+ * keys), and without it sets UP_DEV_TOO_MANY_BLOCKS.  A non-NULL ws that is smaller or misaligned
+ * returns UP_ERR_WORKSPACE before any launch. */
 up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks,
                          const int32_t* cu_seqlens, int R, int64_t T, int64_t nb_cap,
                          int G, int n, int A, double p,
                          uint8_t* block_keep, uint8_t* token_keep, int32_t* kstar,
-                         int32_t* dev_status, void* stream);
+                         void* ws, size_t ws_bytes, int32_t* dev_status, void* stream);
 
 /* Compaction and metadata patch [UP 3.5 "vLLM scheduler integration"]:
  * kept tokens (token_keep != 0) are gathered in ascending packed order (stable), T' of them:
@@ -224,7 +233,7 @@ const char* up_status_string(int code, int device);
 /* Number of kernels this library has launched in this process (for launch accounting). */
 uint64_t up_kernel_launches(void);
 
-/* ABI version of this header: 1. */
+/* ABI version of this header: 2 (up_select_topp takes a workspace). */
 int up_abi_version(void);
 
 #ifdef __cplusplus

@@ -30,12 +30,13 @@ _SIGNATURES = {
     "up_max_blocks": (_i64, [_i32, _i64, _i32]),
     "up_score_workspace_bytes": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32, _i32, _i64, _i32]),
     "up_compact_workspace_bytes": (_sz, [_i32, _i64]),
+    "up_select_workspace_bytes": (_sz, [_i64]),
     "up_workspace_bytes": (_sz, [_i32, _i64, _i32, _i32, _i32, _i32, _i32, _i64]),
     "up_make_cu_blocks": (_i32, [_c_p, _i32, _i64, _i32, _c_p, _c_p, _c_p]),
     "up_score_blocks": (_i32, [_c_p, _c_p, _c_p, _i32, _i64, _i32, _i32, _i32, _i32, _i32, _f32,
                                 _c_p, _i64, _c_p, _c_p, _c_p, _sz, _c_p, _c_p]),
     "up_select_topp": (_i32, [_c_p, _c_p, _c_p, _i32, _i64, _i64, _i32, _i32, _i32, _f64,
-                               _c_p, _c_p, _c_p, _c_p, _c_p]),
+                               _c_p, _c_p, _c_p, _c_p, _sz, _c_p, _c_p]),
     "up_compact": (_i32, [_c_p, _c_p, _i32, _i64, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
                            _c_p, _c_p, _c_p, _c_p, _c_p, _i32, _i32, _c_p, _sz, _c_p, _c_p]),
     "up_compact_noalloc": (_i32, [_c_p, _c_p, _i32, _i64, _c_p, _i32, _c_p, _c_p, _c_p, _c_p, _c_p, _c_p,
@@ -109,6 +110,10 @@ def up_compact_workspace_bytes(R, T):
     return load_library().up_compact_workspace_bytes(R, T)
 
 
+def up_select_workspace_bytes(nb_cap):
+    return load_library().up_select_workspace_bytes(nb_cap)
+
+
 def up_workspace_bytes(R, T, Hq, Hkv, dk, G, n, nb_cap):
     return load_library().up_workspace_bytes(R, T, Hq, Hkv, dk, G, n, nb_cap)
 
@@ -137,10 +142,13 @@ def up_score_blocks(Q, K, cu_seqlens, G, n, cu_blocks, block_scores, ws, dev_sta
 
 
 def up_select_topp(block_scores, cu_blocks, cu_seqlens, T, G, n, A, p, block_keep, token_keep, kstar, dev_status,
-                   stream=None):
+                   ws=None, stream=None):
+    """ws: optional device workspace (up_select_workspace_bytes(block_scores.numel()) bytes); needed only
+    for requests of more than MAX_BLOCKS_PER_REQUEST blocks."""
     R = cu_seqlens.numel() - 1
+    nbytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load_library().up_select_topp(_p(block_scores), _p(cu_blocks), _p(cu_seqlens), R, T, block_scores.numel(),
-                                         G, n, A, float(p), _p(block_keep), _p(token_keep), _p(kstar),
+                                         G, n, A, float(p), _p(block_keep), _p(token_keep), _p(kstar), _p(ws), nbytes,
                                          _p(dev_status), _stream(stream)),
            "up_select_topp")
 

@@ -148,11 +148,13 @@ extern "C" const char* up_status_string(int code, int device) {
 
 extern "C" uint64_t up_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
-extern "C" int up_abi_version(void) { return 1; }
+extern "C" int up_abi_version(void) { return 2; }
 
 extern "C" size_t up_workspace_bytes(int R, int64_t T, int Hq, int Hkv, int dk, int G, int n, int64_t nb_cap) {
     const size_t a = up_score_workspace_bytes(R, T, Hq, Hkv, dk, G, n, nb_cap, 1);
     const size_t b = up_compact_workspace_bytes(R, T);
+    const size_t c = up_select_workspace_bytes(nb_cap);
     if (a == 0 || b == 0) return 0;
-    return a > b ? a : b;
+    const size_t ab = a > b ? a : b;
+    return ab > c ? ab : c;
 }

@@ -3,7 +3,9 @@
 // arXiv 2605.06221, section 3.3 Eq. 5 with the forced sink/window tokens, and the top-p kernel of
 // section 3.5 with the packed sort key of Eq. 14).
 //
-// One CTA per request, everything in shared memory, no CPU round trip:
+// One CTA per request, no CPU round trip.  Requests of at most UP_MAX_BLOCKS_PER_REQUEST blocks keep
+// everything in shared memory; longer ones run the same passes over their keys in the caller's
+// workspace (select_large below):
 //   1. key_g = (phi(b_g) << 32) | g for the request's blocks (phi(x) = bits(x) ^ 0x80000000 for
 //      x >= 0; scores are non-negative sums of probabilities, so the sign bit decides phi).
 //   2. LSD radix sort of the 64-bit keys, descending, 8-bit digits, stable.  The keys are laid out
@@ -63,10 +65,165 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* sh, T* total) {
     return before;
 }
 
+// Token mask of one request: byte i is ranked(i >> log2 G) or a sink (i < A) or a window token
+// (i >= N - n); the aligned interior is written 16 bytes per store (token_keep is 16-byte aligned), the
+// unaligned head and tail byte by byte.
+template <typename RankedFn>
+__device__ __forceinline__ void write_token_mask(uint8_t* token_keep, int c0, int N, int G, int A, int n,
+                                                 RankedFn ranked) {
+    const int tid = threadIdx.x;
+    const int gshift = __ffs(G) - 1;
+    auto keep_byte = [&](int i) -> uint32_t { return (ranked(i >> gshift) || i < A || i >= N - n) ? 1u : 0u; };
+    const int64_t a0 = c0, a1 = (int64_t)c0 + N;
+    const int64_t v0 = min((a0 + 15) & ~int64_t(15), a1), v1 = max(a1 & ~int64_t(15), v0);
+    for (int64_t t = a0 + tid; t < v0; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    for (int64_t t = v1 + tid; t < a1; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    // with the request start 16-byte aligned and G >= 16, a 16-byte group lies in one block; clear
+    // of the sinks and the window it is that block's flag repeated
+    const bool whole = G >= 16 && v0 == a0;
+    for (int64_t t = v0 + 16 * (int64_t)tid; t < v1; t += 16 * (int64_t)kThreads) {
+        const int i0 = static_cast<int>(t - a0);
+        if (whole && i0 >= A && i0 + 15 < N - n) {
+            const uint32_t b = ranked(i0 >> gshift) ? 0x01010101u : 0u;
+            *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(b, b, b, b);
+            continue;
+        }
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = keep_byte(i0 + 4 * q) | (keep_byte(i0 + 4 * q + 1) << 8) | (keep_byte(i0 + 4 * q + 2) << 16) |
+                   (keep_byte(i0 + 4 * q + 3) << 24);
+        *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// Requests of more than UP_MAX_BLOCKS_PER_REQUEST blocks: the keys go through the caller's workspace
+// (two arrays of nb_cap words, this request at offset b0 of each).  The same four stable 8-bit passes
+// over the score word, in tiles of kThreads * kMaxIpt keys: a digit count over the whole request gives
+// each digit's first destination, then the tiles are ranked in (digit, warp, round, lane) order as above
+// and scattered in tile order, so the passes stay stable.  The fp64 prefix sums then run tile by tile
+// with a carry; the total is the last prefix sum, computed in the same order.  Ranked flags go to
+// block_keep, from which the token mask is written; the forced blocks are set last.
+__device__ __noinline__ void select_large(const float* __restrict__ bs, int b0, int nb, int64_t nb_cap, int c0, int N,
+                                          int G, int n, int A, double p, uint64_t* ws_keys, uint8_t* block_keep,
+                                          uint8_t* token_keep, int32_t* kstar, int r, uint8_t* sm, double* shd,
+                                          int* shi, double* s_total, int* s_below) {
+    constexpr int kTileKeys = kThreads * kMaxIpt;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint64_t* src = ws_keys + b0;
+    uint64_t* dst = ws_keys + nb_cap + b0;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(sm);                   // [kRadix digits][kWarps]
+    uint32_t* dbase = hist + kRadix * kWarps;                           // [kRadix] next destination of a digit
+    for (int k = tid; k < nb; k += kThreads) {                          // position k holds block nb - 1 - k
+        const int g = nb - 1 - k;
+        src[k] = pack_key(bs[b0 + g], static_cast<uint32_t>(g));
+    }
+    __syncthreads();
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int ps = 0; ps < 4; ++ps) {
+        const int shift = 32 + 8 * ps;
+        for (int i = tid; i < kRadix; i += kThreads) dbase[i] = 0;
+        __syncthreads();
+        for (int k = tid; k < nb; k += kThreads) atomicAdd(&dbase[static_cast<uint32_t>((~src[k]) >> shift) & 0xFFu], 1u);
+        __syncthreads();
+        {
+            int tot;
+            const int ex = block_exclusive_scan<int>(tid < kRadix ? static_cast<int>(dbase[tid]) : 0, shi, &tot);
+            if (tid < kRadix) dbase[tid] = static_cast<uint32_t>(ex);
+        }
+        __syncthreads();
+        for (int t0 = 0; t0 < nb; t0 += kTileKeys) {
+            for (int i = tid; i < kRadix * kWarps; i += kThreads) hist[i] = 0;
+            __syncthreads();
+            uint32_t rank[kMaxIpt], dig[kMaxIpt];
+            const int base_k = t0 + warp * 32 * kMaxIpt + lane;
+#pragma unroll
+            for (int j = 0; j < kMaxIpt; ++j) {
+                const int k = base_k + 32 * j;
+                const uint32_t d = k < nb ? static_cast<uint32_t>((~src[k]) >> shift) & 0xFFu : 0x100u;   // 0x100: none
+                const uint32_t peers = __match_any_sync(0xffffffffu, d);
+                const uint32_t before = d < 0x100u ? hist[d * kWarps + warp] : 0u;
+                __syncwarp();
+                if (d < 0x100u && (peers & lt_mask) == 0) hist[d * kWarps + warp] = before + __popc(peers);
+                __syncwarp();
+                dig[j] = d;
+                rank[j] = before + __popc(peers & lt_mask);
+            }
+            __syncthreads();
+            if (tid < kRadix) {                 // digit tid: its warps' first destinations in this tile
+                uint32_t run = dbase[tid];
+                for (int w2 = 0; w2 < kWarps; ++w2) {
+                    const uint32_t c = hist[tid * kWarps + w2];
+                    hist[tid * kWarps + w2] = run;
+                    run += c;
+                }
+                dbase[tid] = run;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int j = 0; j < kMaxIpt; ++j)
+                if (dig[j] < 0x100u) dst[hist[dig[j] * kWarps + warp] + rank[j]] = src[base_k + 32 * j];
+            __syncthreads();
+        }
+        uint64_t* t = src;
+        src = dst;
+        dst = t;
+    }
+    // the sorted keys are in src (an even number of passes).  Prefix sums: thread tid of a tile sums the
+    // tile's positions tid * kMaxIpt .. + kMaxIpt - 1 in order, a block scan orders the threads, and the
+    // tiles are chained by a carry that every thread computes identically.
+    auto score_of = [&](int k) {
+        return static_cast<double>(__uint_as_float(static_cast<uint32_t>(src[k] >> 32) ^ 0x80000000u));
+    };
+    auto sweep = [&](bool count, double thr) {
+        double carry = 0.0;
+        int below = 0;
+        for (int t0 = 0; t0 < nb; t0 += kTileKeys) {
+            const int k0 = t0 + tid * kMaxIpt;
+            double part = 0.0;
+            for (int j = 0; j < kMaxIpt; ++j)
+                if (k0 + j < nb) part += score_of(k0 + j);
+            double tot;
+            const double before = block_exclusive_scan<double>(part, shd, &tot);
+            if (count || (k0 <= nb - 1 && nb - 1 < k0 + kMaxIpt)) {
+                double run = carry + before;
+                for (int j = 0; j < kMaxIpt; ++j) {
+                    if (k0 + j < nb) {
+                        run += score_of(k0 + j);
+                        below += run < thr;
+                    }
+                }
+                if (!count && k0 <= nb - 1 && nb - 1 < k0 + kMaxIpt) *s_total = run;
+            }
+            carry += tot;
+        }
+        return below;
+    };
+    sweep(false, 0.0);
+    __syncthreads();
+    const double thr = p * *s_total;
+    const int below = sweep(true, thr);
+    if (tid == 0) *s_below = 0;
+    __syncthreads();
+    if (below) atomicAdd(s_below, below);
+    __syncthreads();
+    const int ks = min(nb, *s_below + 1);
+    for (int k = tid; k < nb; k += kThreads) block_keep[b0 + static_cast<uint32_t>(src[k])] = k < ks ? 1 : 0;
+    __syncthreads();
+    write_token_mask(token_keep, c0, N, G, A, n, [&](int g) { return block_keep[b0 + g] != 0; });
+    __syncthreads();
+    for (int g = tid; g < nb; g += kThreads) {
+        const bool forced = (static_cast<int64_t>(g) * G < A) || (static_cast<int64_t>(g + 1) * G > static_cast<int64_t>(N) - n);
+        if (forced) block_keep[b0 + g] = 1;
+    }
+    if (tid == 0) kstar[r] = ks;
+}
+
 __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restrict__ bs, const int32_t* __restrict__ cb,
                                                           const int32_t* __restrict__ cu, int R, int T, int64_t nb_cap,
                                                           int G, int n, int A, double p, uint8_t* block_keep,
-                                                          uint8_t* token_keep, int32_t* kstar, int32_t* status) {
+                                                          uint8_t* token_keep, int32_t* kstar, uint64_t* ws_keys,
+                                                          int32_t* status) {
     pdl_wait();
     pdl_trigger();
     extern __shared__ __align__(16) uint8_t sm[];
@@ -88,7 +245,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
         int bad = 0;
         if ((r == 0 && c0 != 0) || c1 < c0 || c1 > T || (r == R - 1 && c1 != T)) bad = UP_DEV_BAD_CU_SEQLENS;
         else if ((r == 0 && cb[0] != 0) || cb[r + 1] - cb[r] != nb || (int64_t)cb[r + 1] > nb_cap) bad = UP_DEV_BAD_CU_BLOCKS;
-        else if (nb > UP_MAX_BLOCKS_PER_REQUEST) bad = UP_DEV_TOO_MANY_BLOCKS;
+        else if (nb > UP_MAX_BLOCKS_PER_REQUEST && ws_keys == nullptr) bad = UP_DEV_TOO_MANY_BLOCKS;
         s_bad = bad;
         if (bad) set_status(status, bad);
     }
@@ -99,6 +256,11 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
         return;
     }
     const int b0 = cb[r];
+    if (nb > UP_MAX_BLOCKS_PER_REQUEST) {
+        select_large(bs, b0, nb, nb_cap, c0, N, G, n, A, p, ws_keys, block_keep, token_keep, kstar, r, sm, shd, shi,
+                     &s_total, &s_below);
+        return;
+    }
     const int ipt = (nb + kThreads - 1) / kThreads;      // keys per thread
     const int npad = ipt * kThreads;
 
@@ -231,31 +393,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
         const bool forced = (static_cast<int64_t>(g) * G < A) || (static_cast<int64_t>(g + 1) * G > static_cast<int64_t>(N) - n);
         block_keep[b0 + g] = (ranked[g] || forced) ? 1 : 0;
     }
-    // token mask: byte i of the request is ranked[i >> log2 G] or a sink (i < A) or window (i >= N - n);
-    // the aligned interior is written 16 bytes per store, the unaligned head and tail byte by byte
-    const int gshift = __ffs(G) - 1;
-    auto keep_byte = [&](int i) -> uint32_t { return (ranked[i >> gshift] || i < A || i >= N - n) ? 1u : 0u; };
-    const int64_t a0 = c0, a1 = (int64_t)c0 + N;
-    const int64_t v0 = min((a0 + 15) & ~int64_t(15), a1), v1 = max(a1 & ~int64_t(15), v0);
-    for (int64_t t = a0 + tid; t < v0; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
-    for (int64_t t = v1 + tid; t < a1; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
-    // with the request start 16-byte aligned and G >= 16, a 16-byte group lies in one block; clear
-    // of the sinks and the window it is that block's flag repeated
-    const bool whole = G >= 16 && v0 == a0;
-    for (int64_t t = v0 + 16 * (int64_t)tid; t < v1; t += 16 * (int64_t)kThreads) {
-        const int i0 = static_cast<int>(t - a0);
-        if (whole && i0 >= A && i0 + 15 < N - n) {
-            const uint32_t b = ranked[i0 >> gshift] ? 0x01010101u : 0u;
-            *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(b, b, b, b);
-            continue;
-        }
-        uint32_t w[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-            w[q] = keep_byte(i0 + 4 * q) | (keep_byte(i0 + 4 * q + 1) << 8) | (keep_byte(i0 + 4 * q + 2) << 16) |
-                   (keep_byte(i0 + 4 * q + 3) << 24);
-        *reinterpret_cast<uint4*>(token_keep + t) = make_uint4(w[0], w[1], w[2], w[3]);
-    }
+    write_token_mask(token_keep, c0, N, G, A, n, [&](int g) { return ranked[g] != 0; });
     if (tid == 0) kstar[r] = ks;
 }
 
@@ -324,10 +462,15 @@ extern "C" up_status up_make_cu_blocks(const int32_t* cu_seqlens, int R, int64_t
     return check_launch();
 }
 
+extern "C" size_t up_select_workspace_bytes(int64_t nb_cap) {
+    if (nb_cap < 0) return 0;
+    return align_up(sizeof(uint64_t) * 2 * static_cast<size_t>(nb_cap), 256);
+}
+
 extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu_blocks, const int32_t* cu_seqlens,
                                     int R, int64_t T, int64_t nb_cap, int G, int n, int A, double p,
-                                    uint8_t* block_keep, uint8_t* token_keep, int32_t* kstar, int32_t* dev_status,
-                                    void* stream) {
+                                    uint8_t* block_keep, uint8_t* token_keep, int32_t* kstar, void* ws,
+                                    size_t ws_bytes, int32_t* dev_status, void* stream) {
     // token_keep may be NULL for a batch without tokens (T = 0)
     if (!block_scores || !cu_blocks || !cu_seqlens || !block_keep || (T > 0 && !token_keep) || !kstar || !dev_status)
         return UP_ERR_ARG;
@@ -335,6 +478,7 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
     if (!(p > 0.0) || !(p <= 1.0)) return UP_ERR_ARG;
     if (G & (G - 1)) return UP_ERR_SHAPE;          // block size must be a power of two
     if (T > 0 && !aligned16(token_keep)) return UP_ERR_SHAPE;   // the mask is written 16 bytes per store
+    if (ws != nullptr && (!aligned16(ws) || ws_bytes < up_select_workspace_bytes(nb_cap))) return UP_ERR_WORKSPACE;
     static int attr_done[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return UP_ERR_CUDA;
@@ -346,7 +490,7 @@ extern "C" up_status up_select_topp(const float* block_scores, const int32_t* cu
     }
     launch_pdl(select::select_kernel, dim3(R), dim3(select::kThreads), select::kSmemBytes,
         static_cast<cudaStream_t>(stream), block_scores, cu_blocks, cu_seqlens, R, static_cast<int>(T), nb_cap, G, n, A, p, block_keep, token_keep,
-        kstar, dev_status);
+        kstar, static_cast<uint64_t*>(ws), dev_status);
     count_launch();
     return check_launch();
 }

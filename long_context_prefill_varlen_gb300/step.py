@@ -10,7 +10,8 @@ from __future__ import annotations
 import torch
 
 from . import (up_compact, up_compact_workspace_bytes, up_make_cu_blocks, up_max_blocks, up_read_status,
-               up_scatter_back, up_score_blocks, up_score_workspace_bytes, up_select_topp, up_seqused)
+               up_scatter_back, up_score_blocks, up_score_workspace_bytes, up_select_topp, up_select_workspace_bytes,
+               up_seqused)
 
 
 class DropStep:
@@ -41,10 +42,11 @@ class DropStep:
         self.kept_len = torch.zeros(L, R, **i32)
         self.drop_layer = torch.zeros(L, device=dev, dtype=torch.uint8)
         self.seqused_out = torch.zeros(R, **i32)
-        ws = max(up_score_workspace_bytes(R, T, Hq, Hkv, dk, G, n, self.nb_cap, with_token_scores),
-                 up_compact_workspace_bytes(R, T))
-        if ws == 0:
+        sws = up_score_workspace_bytes(R, T, Hq, Hkv, dk, G, n, self.nb_cap, with_token_scores)
+        if sws == 0:
             raise ValueError("unsupported geometry for up_score_blocks")
+        # one workspace for the calls of the step, which run one after another on a stream
+        ws = max(sws, up_compact_workspace_bytes(R, T), up_select_workspace_bytes(self.nb_cap))
         self.ws = torch.empty(ws, device=dev, dtype=torch.uint8)
         up_make_cu_blocks(self.cu, G, self.cu_blocks, self.status, T=T)
 
@@ -54,7 +56,7 @@ class DropStep:
 
     def select(self, stream=None):
         up_select_topp(self.block_scores, self.cu_blocks, self.cu, self.T, self.G, self.n, self.A, self.p,
-                       self.block_keep, self.token_keep, self.kstar, self.status, stream=stream)
+                       self.block_keep, self.token_keep, self.kstar, self.status, ws=self.ws, stream=stream)
 
     def compact(self, hidden=None, positions=None, slots=None, stream=None):
         up_compact(self.token_keep, self.cu, self.kept_index, self.new_cu, self.new_len, self.num_actual, self.ws,

@@ -37,7 +37,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_sizing_helpers(lib):
     import long_context_prefill_varlen_gb300 as up
-    assert up.up_abi_version() == 1
+    assert up.up_abi_version() == 2
     assert up.up_max_blocks(3, 1000, 64) == 1000 // 64 + 3
     nb = up.up_max_blocks(1, 32768, 64)
     a = up.up_score_workspace_bytes(1, 32768, 32, 8, 128, 64, 128, nb)
@@ -47,7 +47,9 @@ def test_sizing_helpers(lib):
     assert up.up_score_workspace_bytes(1, 32768, 30, 8, 128, 64, 128, nb) == 0     # Hq % Hkv != 0
     assert up.up_score_workspace_bytes(1, 32768, 32, 8, 128, 64, 48, nb) == 0      # n must divide 128
     assert up.up_compact_workspace_bytes(4, 10_000) > 0
-    assert up.up_workspace_bytes(1, 32768, 32, 8, 128, 64, 128, nb) >= max(b, up.up_compact_workspace_bytes(1, 32768))
+    assert up.up_select_workspace_bytes(nb) >= 16 * nb
+    assert up.up_workspace_bytes(1, 32768, 32, 8, 128, 64, 128, nb) >= max(b, up.up_compact_workspace_bytes(1, 32768),
+                                                                         up.up_select_workspace_bytes(nb))
 
 
 def test_host_validation_returns_before_any_launch(lib):
@@ -66,13 +68,15 @@ def test_host_validation_returns_before_any_launch(lib):
     s = lib.up_score_blocks(fake, fake, fake, 1, 4096, 32, 8, 128, 64, 128, 0.088, fake, 64, fake, null, fake,
                             16, fake, null)
     assert s == up.UP_ERR_WORKSPACE
-    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 1.5, fake, fake, fake, fake, null)
+    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 1.5, fake, fake, fake, null, 0, fake, null)
     assert s == up.UP_ERR_ARG                      # p outside (0, 1]
-    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.0, fake, fake, fake, fake, null)
+    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.0, fake, fake, fake, null, 0, fake, null)
     assert s == up.UP_ERR_ARG
     odd = ctypes.c_void_p(0x1001)      # a token mask that is not 16-byte aligned (a view at an odd offset)
-    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.99, fake, odd, fake, fake, null)
+    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.99, fake, odd, fake, null, 0, fake, null)
     assert s == up.UP_ERR_SHAPE
+    s = lib.up_select_topp(fake, fake, fake, 1, 4096, 64, 64, 128, 128, 0.99, fake, fake, fake, fake, 64, fake, null)
+    assert s == up.UP_ERR_WORKSPACE                # a workspace smaller than up_select_workspace_bytes
     s = lib.up_compact(fake, fake, 1, 4096, fake, 12, null, null, fake, null, null, fake, fake, fake, fake, null,
                        null, 0, 0, fake, 1 << 20, fake, null)
     assert s == up.UP_ERR_SHAPE                    # hidden size must be a multiple of 8

@@ -85,7 +85,7 @@ def test_select_matches_oracle_on_the_same_scores(kind, p):
     assert np.array_equal(tk.cpu().numpy(), ref["token_keep"])
 
 
-def test_select_rejects_a_request_with_too_many_blocks():
+def test_select_without_a_workspace_rejects_a_request_over_the_shared_memory_limit():
     G, N = 16, 16 * (up.MAX_BLOCKS_PER_REQUEST + 1)
     cu = np.array([0, N], dtype=np.int32)
     nb = up.up_max_blocks(1, N, G)
@@ -95,6 +95,42 @@ def test_select_rejects_a_request_with_too_many_blocks():
                       torch.zeros(nb, dtype=torch.uint8, device="cuda"), torch.zeros(N, dtype=torch.uint8, device="cuda"),
                       torch.zeros(1, dtype=torch.int32, device="cuda"), st)
     assert up.up_read_status(st) == 3
+
+
+# requests of more than MAX_BLOCKS_PER_REQUEST blocks sort their keys through the workspace (tiles of
+# 8192 keys); next to them, short requests take the shared-memory path in the same launch
+@pytest.mark.parametrize("kind", ["zipf", "ties", "uniform", "dominant"])
+@pytest.mark.parametrize("p", [0.5, 0.99, 1.0])
+@pytest.mark.parametrize("G", [64, 16])
+def test_select_beyond_the_shared_memory_limit_matches_oracle(kind, p, G):
+    rng = np.random.default_rng(hash((kind, p, G, "large")) % 2**32)
+    n, A = 128, 128
+    if G == 64:
+        lengths = [64 * 16384, 5000, 64 * 65536 + 17, 300, 64 * 8193]
+    else:
+        lengths = [16 * 20000 + 3, 0, 16 * 8192]
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32)
+    T = int(cu[-1])
+    scores = np.concatenate(_score_vectors(rng, lengths, G, kind)).astype(np.float32)
+    cb = oracle.cu_blocks_of(cu, G)
+    nb_cap = up.up_max_blocks(len(lengths), T, G)
+    bs = torch.zeros(nb_cap, dtype=torch.float32, device="cuda")
+    bs[:len(scores)] = torch.from_numpy(scores).cuda()
+    ws = torch.empty(up.up_select_workspace_bytes(nb_cap), dtype=torch.uint8, device="cuda")
+    ref = oracle.select(scores.astype(np.float64), cu, G, n, A, p)
+    outs = []
+    for _ in range(2):                       # deterministic, and nothing depends on the workspace's contents
+        bk = torch.zeros(nb_cap, dtype=torch.uint8, device="cuda")
+        tk = torch.zeros(T, dtype=torch.uint8, device="cuda")
+        ks = torch.zeros(len(lengths), dtype=torch.int32, device="cuda")
+        st = _status()
+        up.up_select_topp(bs, _i32(cb), _i32(cu), T, G, n, A, p, bk, tk, ks, st, ws=ws)
+        assert up.up_read_status(st) == 0
+        assert np.array_equal(ks.cpu().numpy(), ref["kstar"])
+        assert np.array_equal(bk.cpu().numpy()[:cb[-1]], ref["block_keep"])
+        assert np.array_equal(tk.cpu().numpy(), ref["token_keep"])
+        outs.append(tk)
+        ws.fill_(0xAB)
 
 
 # ------------------------------------------------------------------------------------------ compaction, Eq. 8, 16, 17
