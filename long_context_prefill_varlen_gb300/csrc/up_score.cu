@@ -191,11 +191,18 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sh, int* to
     return before;
 }
 
-__global__ void __launch_bounds__(1024) plan_kernel(Params P) {
+// Up to this many requests every plan CTA keeps each request's first run-0 item in shared memory and
+// the item list is written by a grid of CTAs; beyond it one CTA writes the list (searching the
+// unit offsets in global memory).
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemReqs = 4096;
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
     pdl_wait();
     pdl_trigger();
     __shared__ int s_bad;
     __shared__ int s_scan[32];
+    __shared__ int s_first[kPlanSmemReqs];
     const int tid = threadIdx.x;
     if (tid == 0) s_bad = 0;
     __syncthreads();
@@ -208,13 +215,15 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     }
     __syncthreads();
     if (s_bad) {
-        if (tid == 0) {
+        if (tid == 0 && blockIdx.x == 0) {
             set_status(P.status, (s_bad & 1) ? UP_DEV_BAD_CU_SEQLENS : UP_DEV_BAD_CU_BLOCKS);
             P.n_items[0] = 0;
             P.n_items[1] = 0;      // metadata invalid: finalize writes nothing
         }
         return;
     }
+    const int NS = P.nsets;
+    const bool in_smem = P.R <= kPlanSmemReqs;
     const int per = (P.R + blockDim.x - 1) / blockDim.x;
     const int r0 = min(P.R, tid * per), r1 = min(P.R, r0 + per);
     auto nitems = [&](int r) {
@@ -228,10 +237,13 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     int off = block_exclusive_scan_1024(local, s_scan, &total);
     for (int r = r0; r < r1; ++r) {
         const int ni = nitems(r);
-        for (int kk = 0; kk < P.units_per_req; ++kk) {
-            const int u = r * P.units_per_req + kk;
-            P.unit_items[u] = make_int2(off + kk * ni, ni);
+        if (blockIdx.x == 0) {
+            for (int kk = 0; kk < P.units_per_req; ++kk) {
+                const int u = r * P.units_per_req + kk;
+                P.unit_items[u] = make_int2(off + kk * ni, ni);
+            }
         }
+        if (in_smem) s_first[r] = off / NS;
         off += ni * P.units_per_req;
     }
     __syncthreads();
@@ -245,9 +257,9 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
     // KV heads of a token range are also read together (whole rows of the [T, Hkv, d_k] K tensor).
     // A unit's items are therefore not contiguous in the list; its pass-1 partials are indexed by the
     // item's tile pair inside the unit (unit_items[u].x + pair).  nsets = 1 is the plain order.
-    const int NS = P.nsets;
     const int run = total / NS;
-    for (int it = tid; it < total; it += blockDim.x) {
+    auto first = [&](int r) { return in_smem ? s_first[r] : P.unit_items[r * P.units_per_req].x / NS; };
+    for (int it = blockIdx.x * blockDim.x + tid; it < total; it += gridDim.x * blockDim.x) {
         const int set = it / run, rel = it - set * run;
         // the request: the largest r whose first run-0 item (its first item / NS) is <= rel; never an
         // empty request (an empty request shares its first item with the next one, and rel < run
@@ -255,18 +267,18 @@ __global__ void __launch_bounds__(1024) plan_kernel(Params P) {
         int lo = 0, hi = P.R;
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (P.unit_items[mid * P.units_per_req].x / NS <= rel) lo = mid; else hi = mid;
+            if (first(mid) <= rel) lo = mid; else hi = mid;
         }
         const int r = lo;
         const int ni = nitems(r);
-        const int rel2 = rel - P.unit_items[r * P.units_per_req].x / NS;
+        const int rel2 = rel - first(r);
         const int kq = rel2 / ni, sidx = rel2 % ni;
         const int kk = kq * NS + set;
         const int N = P.cu[r + 1] - P.cu[r];
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
         P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
     }
-    if (tid == 0) {
+    if (tid == 0 && blockIdx.x == 0) {
         P.n_items[0] = total;
         P.n_items[1] = 1;          // metadata validated
     }
@@ -1266,21 +1278,31 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
     const int upr = P.units_per_req, rows = P.slab_rows, rows4 = rows / 4;
     const int pairs = upr * rows4;
     const int req_items = __ldcg(P.n_items) / upr;          // items of unit 0 of every request
-    for (int task = blockIdx.x; task < req_items * kItemTiles; task += gridDim.x) {
-        // the request: the largest r whose first item (unit_items[r * upr].x / upr) is <= task / 2
-        const int ri = task / kItemTiles;
-        int lo = 0, hi = P.R;
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (P.unit_items[mid * upr].x / upr <= ri) lo = mid; else hi = mid;
+    // each CTA takes a contiguous range of (request, key tile) tasks; the request changes rarely inside it
+    const int tasks = req_items * kItemTiles;
+    const int per = (tasks + gridDim.x - 1) / gridDim.x;
+    const int task0 = blockIdx.x * per, task1 = min(tasks, task0 + per);
+    int r = -1, rbeg = 0, rend = 0, N = 0;
+    for (int task = task0; task < task1; ++task) {
+        if (task >= rend) {
+            // the request: the largest r whose first item (unit_items[r * upr].x / upr) is <= task / 2
+            const int ri = task / kItemTiles;
+            int lo = 0, hi = P.R;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (P.unit_items[mid * upr].x / upr <= ri) lo = mid; else hi = mid;
+            }
+            r = lo;
+            N = P.cu[r + 1] - P.cu[r];
+            rbeg = (P.unit_items[r * upr].x / upr) * kItemTiles;
+            rend = rbeg + P.unit_items[r * upr].y * kItemTiles;
+            __syncthreads();                                    // the previous request's bases are no longer read
+            for (int kk = threadIdx.x; kk < upr; kk += kReduceThreads)
+                s_tile0[kk] = P.unit_items[r * upr + kk].x * kItemTiles;
+            __syncthreads();
         }
-        const int r = lo;
-        const int N = P.cu[r + 1] - P.cu[r];
-        const int tile = task - (P.unit_items[r * upr].x / upr) * kItemTiles;
+        const int tile = task - rbeg;
         if (N == 0 || tile * kTileKeys >= N) continue;     // the odd tile of a request's last item
-        for (int kk = threadIdx.x; kk < upr; kk += kReduceThreads)
-            s_tile0[kk] = P.unit_items[r * upr + kk].x * kItemTiles + tile;
-        __syncthreads();
         float acc[SPT];
 #pragma unroll
         for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
@@ -1291,7 +1313,7 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
                 const int i = i0 + b * kReduceThreads;
                 if (i < pairs) {
                     const int kk = i / rows4, r0 = (i - kk * rows4) * 4;
-                    const size_t t = static_cast<size_t>(s_tile0[kk]);
+                    const size_t t = static_cast<size_t>(s_tile0[kk]) + tile;
                     const float4 m4 = ldcg4(P.bm + t * rows + r0);
                     const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
 #pragma unroll
@@ -1490,7 +1512,11 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.status = dev_status;
     P.nsets = work_sets(P.units_per_req, g.slabs, num_sms());
 
-    cudaError_t le = launch_pdl(plan_kernel, dim3(1), dim3(1024), 0, st, P);
+    // the item list by a grid of CTAs (one while the requests' offsets do not fit their shared memory)
+    const int pgrid = R <= kPlanSmemReqs
+                          ? static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(L.items_cap, kPlanThreads), num_sms())))
+                          : 1;
+    cudaError_t le = launch_pdl(plan_kernel, dim3(pgrid), dim3(kPlanThreads), 0, st, P);
     count_launch();
     if (le != cudaSuccess) return UP_ERR_CUDA;
     if (T > 0) {
