@@ -65,6 +65,7 @@ typedef enum {
 #define UP_DEV_WAIT_TIMEOUT     4   /* a pipeline wait inside a kernel ran past its time bound    */
 #define UP_DEV_BAD_POSITION     5   /* Eq. 16: a position beyond its block-table row (slot = -1) */
 #define UP_DEV_BAD_TOKEN_COUNT  6   /* num_actual_tokens outside [0, T_upper]                     */
+#define UP_DEV_BOUNDS           7   /* bounds-checked build only: an index outside its array      */
 
 #define UP_MAX_BLOCKS_PER_REQUEST 8192   /* up to this many blocks up_select_topp sorts a request in
                                             shared memory; longer requests need its workspace */
@@ -235,6 +236,11 @@ uint64_t up_kernel_launches(void);
 
 /* ABI version of this header: 2 (up_select_topp takes a workspace). */
 int up_abi_version(void);
+
+/* 1 in the bounds-checked build of the library (compiled with -DUP_DEBUG_BOUNDS, a development aid:
+ * every kernel checks each global index against its array's length, records UP_DEV_BOUNDS in the
+ * status word on a violation and skips the access), 0 in the normal build. */
+int up_debug_bounds(void);
 
 #ifdef __cplusplus
 }

@@ -48,6 +48,7 @@ _SIGNATURES = {
     "up_status_string": (ctypes.c_char_p, [_i32, _i32]),
     "up_kernel_launches": (_u64, []),
     "up_abi_version": (_i32, []),
+    "up_debug_bounds": (_i32, []),
 }
 
 _lib = None
@@ -229,6 +230,10 @@ def up_kernel_launches():
 
 def up_abi_version():
     return int(load_library().up_abi_version())
+
+
+def up_debug_bounds():
+    return int(load_library().up_debug_bounds())
 
 
 from .step import DropStep  # noqa: E402,F401

@@ -91,14 +91,15 @@ __device__ __forceinline__ int block_reduce(int v, int* sh) {
     return t;
 }
 
-__global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __restrict__ keep, int T, int* tile_cnt) {
+__global__ void __launch_bounds__(kTileThreads) count_kernel(const uint8_t* __restrict__ keep, int T, int* tile_cnt,
+                                                              int tiles, int32_t* status) {
     pdl_wait();
     pdl_trigger();
     __shared__ int sh[9];
     const int64_t t0 = (int64_t)blockIdx.x * kTile + threadIdx.x * 16;
     const int c = t0 < T ? count_nonzero_bytes(load_flags16(keep, t0, T)) : 0;
     const int tot = block_reduce(c, sh);
-    if (threadIdx.x == 0) tile_cnt[blockIdx.x] = tot;
+    if (threadIdx.x == 0 && UP_IN(blockIdx.x, tiles, status)) tile_cnt[blockIdx.x] = tot;
 }
 
 // Whether cu_seqlens is a non-decreasing 0..T sequence (all threads of the CTA take part; sh_bad is
@@ -118,28 +119,29 @@ __device__ __forceinline__ bool cu_valid(const int32_t* __restrict__ cu, int R, 
 // total = kept tokens of the stream): kept tokens before each request boundary (one warp per
 // boundary; the boundary's partial tile is counted flag by flag) -> new_cu_seqlens, new_seq_lens,
 // num_actual_tokens and the drop history.  Called by every thread of one CTA, cu_seqlens valid.
-__device__ void request_metadata(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu, int R, int tiles,
-                                 const int* off, int total, int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
-                                 int32_t* kept_len, uint8_t* drop_layer, int layer) {
+__device__ void request_metadata(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu, int R, int T,
+                                 int tiles, const int* off, int total, int32_t* new_cu, int32_t* new_len,
+                                 int32_t* num_actual, int32_t* kept_len, uint8_t* drop_layer, int L, int layer,
+                                 int32_t* status) {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     for (int r = w; r <= R; r += nw) {
         const int x0 = cu[r];
         const int tile = x0 / kTile;
         int c = 0;
-        for (int t = tile * kTile + lane; t < x0; t += 32) c += keep[t] != 0;
+        for (int t = tile * kTile + lane; t < x0; t += 32) c += (UP_IN(t, T, status) ? keep[t] : 0) != 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-        if (lane == 0) new_cu[r] = (tile < tiles ? off[tile] : total) + c;
+        if (lane == 0 && UP_IN(r, R + 1, status)) new_cu[r] = (tile < tiles ? off[tile] : total) + c;
     }
     __syncthreads();
     for (int r = threadIdx.x; r < R; r += blockDim.x) {
         const int len = new_cu[r + 1] - new_cu[r];
         new_len[r] = len;
-        if (kept_len) kept_len[(int64_t)layer * R + r] = len;
+        if (kept_len && UP_IN((int64_t)layer * R + r, (int64_t)L * R, status)) kept_len[(int64_t)layer * R + r] = len;
     }
     if (threadIdx.x == 0) {
         *num_actual = new_cu[R];
-        if (drop_layer) drop_layer[layer] = 1;
+        if (drop_layer && UP_IN(layer, L, status)) drop_layer[layer] = 1;
     }
 }
 
@@ -150,7 +152,7 @@ __device__ void request_metadata(const uint8_t* __restrict__ keep, const int32_t
 __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ keep, const int32_t* __restrict__ cu,
                                                     int R, int T, int* tile_cnt, int* tile_off,
                                                     int32_t* new_cu, int32_t* new_len, int32_t* num_actual,
-                                                    int32_t* kept_len, uint8_t* drop_layer, int layer,
+                                                    int32_t* kept_len, uint8_t* drop_layer, int L, int layer,
                                                     int32_t* status, int count_here) {
     pdl_wait();
     pdl_trigger();
@@ -173,7 +175,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
             }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) c += __shfl_xor_sync(0xffffffffu, c, o);
-            if (lane == 0) tile_cnt[i] = c;
+            if (lane == 0 && UP_IN(i, tiles, status)) tile_cnt[i] = c;
         }
         __syncthreads();
     }
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
     const int per = (tiles + blockDim.x - 1) / blockDim.x;
     const int a0 = min(tiles, tid * per), a1 = min(tiles, a0 + per);
     int local = 0;
-    for (int i = a0; i < a1; ++i) local += tile_cnt[i];
+    for (int i = a0; i < a1; ++i) local += UP_IN(i, tiles, status) ? tile_cnt[i] : 0;
     int x = local;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -203,15 +205,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint8_t* __restrict__ 
     const int total = sh[31];
     int off = (w > 0 ? sh[w - 1] : 0) + x - local;
     for (int i = a0; i < a1; ++i) {
+        if (!UP_IN(i, tiles, status)) continue;
         tile_off[i] = off;
         off += tile_cnt[i];
     }
     __syncthreads();
     if (!ok) return;
-    request_metadata(keep, cu, R, tiles, tile_off, total, new_cu, new_len, num_actual, kept_len, drop_layer, layer);
+    request_metadata(keep, cu, R, T, tiles, tile_off, total, new_cu, new_len, num_actual, kept_len, drop_layer, L, layer,
+                     status);
 }
 
-// One warp copies one row of V 16-byte vectors, kRowUnroll loads in flight per lane.
+// One warp copies one row of V 16-byte vectors, kRowUnroll loads in flight per lane.  In the
+// bounds-checked build the callers check the two row indices first.
 __device__ __forceinline__ void copy_row(const uint4* __restrict__ s, uint4* __restrict__ d, int V, int lane) {
     int j = lane;
     for (; j + 32 * (kRowUnroll - 1) < V; j += 32 * kRowUnroll) {
@@ -231,7 +236,7 @@ __device__ __forceinline__ void copy_row(const uint4* __restrict__ s, uint4* __r
 // Metadata outputs of a gather that scans the stream itself (SELF).
 struct MetaOut {
     const int32_t* cu;
-    int R, layer;
+    int R, L, layer;
     int32_t *new_cu, *new_len, *num_actual, *kept_len, *status;
     uint8_t* drop_layer;
 };
@@ -284,8 +289,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* _
         __syncthreads();
         if (blockIdx.x == 0) {
             if (cu_valid(M.cu, M.R, T, &s_bad))
-                request_metadata(keep, M.cu, M.R, tiles, s_off, s_total, M.new_cu, M.new_len, M.num_actual,
-                                 M.kept_len, M.drop_layer, M.layer);
+                request_metadata(keep, M.cu, M.R, T, tiles, s_off, s_total, M.new_cu, M.new_len, M.num_actual,
+                                 M.kept_len, M.drop_layer, M.L, M.layer, M.status);
             else if (tid == 0) {
                 set_status(M.status, UP_DEV_BAD_CU_SEQLENS);
                 *M.num_actual = 0;
@@ -321,10 +326,11 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* _
 #pragma unroll
         for (int i = 0; i < kTileThreads / 32; ++i) cnt += s_wsum[i];
         __syncthreads();
-        const int base = SELF ? s_off[tile] : tile_off[tile];
+        const int base = SELF ? s_off[tile] : (UP_IN(tile, tiles, M.status) ? tile_off[tile] : 0);
         if (part == 0) {
             for (int k = tid; k < cnt; k += kGatherThreads) {
                 const int sidx = s_src[k];
+                if (!UP_IN(base + k, T, M.status) || !UP_IN(sidx, T, M.status)) continue;
                 kept_index[base + k] = sidx;
                 if (out_pos) out_pos[base + k] = pos[sidx];
                 if (out_slots) out_slots[base + k] = slots[sidx];
@@ -334,7 +340,8 @@ __global__ void __launch_bounds__(kGatherThreads) gather_kernel(const uint8_t* _
             const int per = (cnt + parts - 1) / parts;
             const int k0 = part * per, k1 = min(cnt, k0 + per);
             for (int k = k0 + w; k < k1; k += kGatherThreads / 32)
-                copy_row(src + (int64_t)s_src[k] * V, dst + (int64_t)(base + k) * V, V, lane);
+                if (UP_IN(s_src[k], T, M.status) && UP_IN(base + k, T, M.status))
+                    copy_row(src + (int64_t)s_src[k] * V, dst + (int64_t)(base + k) * V, V, lane);
         }
     }
 }
@@ -356,6 +363,8 @@ __global__ void __launch_bounds__(kRowThreads) rows_kernel(const uint4* __restri
     const int warps = gridDim.x * (kRowThreads / 32);
     for (int k = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); k < n; k += warps) {
         const int64_t other = idx[k];
+        // the residual's row count is not an argument: the bounds-checked build checks the sign only
+        if (!UP_IN(other, int64_t(1) << 31, status)) continue;
         copy_row(src + (GATHER ? other : (int64_t)k) * V, dst + (GATHER ? (int64_t)k : other) * V, V, lane);
     }
 }
@@ -412,9 +421,9 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
                               int hdim, const int64_t* positions, const int64_t* slots, uint16_t* out_hidden,
                               int64_t* out_positions, int64_t* out_slots, int32_t* kept_index, int32_t* new_cu,
                               int32_t* new_len, int32_t* num_actual, int32_t* kept_len, uint8_t* drop_layer,
-                              int layer, int* tile_cnt, int* tile_off, int32_t* status, cudaStream_t st) {
+                              int L, int layer, int* tile_cnt, int* tile_off, int32_t* status, cudaStream_t st) {
     const int tiles = static_cast<int>(cdiv(Ti, kTile));
-    const MetaOut M{cu, R, layer, new_cu, new_len, num_actual, kept_len, status, drop_layer};
+    const MetaOut M{cu, R, L, layer, new_cu, new_len, num_actual, kept_len, status, drop_layer};
     if (tiles <= kSelfScanTiles) {        // one launch: the gather scans the short stream itself
         launch_gather<true>(keep, Ti, tiles, nullptr, hidden, hdim, positions, slots, out_hidden, out_positions,
                             out_slots, kept_index, M, st);
@@ -422,11 +431,11 @@ static void launch_compaction(const uint8_t* keep, const int32_t* cu, int R, int
     }
     const int count_here = tiles <= kScanCountTiles ? 1 : 0;
     if (!count_here) {
-        launch_pdl(count_kernel, dim3(tiles), dim3(kTileThreads), 0, st, keep, Ti, tile_cnt);
+        launch_pdl(count_kernel, dim3(tiles), dim3(kTileThreads), 0, st, keep, Ti, tile_cnt, tiles, status);
         count_launch();
     }
     launch_pdl(scan_kernel, dim3(1), dim3(1024), 0, st,
-        keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len, drop_layer, layer, status,
+        keep, cu, R, Ti, tile_cnt, tile_off, new_cu, new_len, num_actual, kept_len, drop_layer, L, layer, status,
         count_here);
     count_launch();
     launch_gather<false>(keep, Ti, tiles, tile_off, hidden, hdim, positions, slots, out_hidden, out_positions,
@@ -467,7 +476,7 @@ extern "C" up_status up_compact(const uint8_t* token_keep, const int32_t* cu_seq
     int* tile_off = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + Lw.tile_off);
     compact::launch_compaction(token_keep, cu_seqlens, R, static_cast<int>(T), hidden, hdim, positions, slots,
                                out_hidden, out_positions, out_slots, kept_index, new_cu_seqlens, new_seq_lens,
-                               num_actual_tokens, kept_len, drop_layer, layer, tile_cnt, tile_off, dev_status, st);
+                               num_actual_tokens, kept_len, drop_layer, L, layer, tile_cnt, tile_off, dev_status, st);
     return check_launch();
 }
 
@@ -560,7 +569,7 @@ extern "C" up_status up_compact_noalloc(const uint8_t* token_keep, const int32_t
     int* tile_off = scratch + compact::kNoAllocMaxTiles + 1;
     compact::launch_compaction(token_keep, cu_seqlens, R, static_cast<int>(T), hidden, hdim, positions, slots,
                                out_hidden, out_positions, out_slots, kept_index, new_cu_seqlens, new_seq_lens,
-                               num_actual_tokens, kept_len, drop_layer, layer, tile_cnt, tile_off, dev_status,
+                               num_actual_tokens, kept_len, drop_layer, L, layer, tile_cnt, tile_off, dev_status,
                                static_cast<cudaStream_t>(stream));
     return check_launch();
 }

@@ -48,6 +48,22 @@ __device__ __forceinline__ void set_status(int32_t* st, int code) {
     if (st) atomicCAS(st, 0, code);
 }
 
+// Bounds-checked build (-DUP_DEBUG_BOUNDS): UP_IN(i, n, st) is true when 0 <= i < n; otherwise it
+// records UP_DEV_BOUNDS in the status word st (if there is one) and the caller skips the access.  In
+// the normal build it is the constant true and costs nothing.  Every global index of the library's
+// kernels goes through it: `x = UP_IN(i, n, st) ? p[i] : 0` for loads, `if (UP_IN(i, n, st)) p[i] = v`
+// for stores.
+#ifdef UP_DEBUG_BOUNDS
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, int32_t* st) {
+    if (i >= 0 && i < n) return true;
+    set_status(st, UP_DEV_BOUNDS);
+    return false;
+}
+#define UP_IN(i, n, st) (::up::in_bounds(static_cast<int64_t>(i), static_cast<int64_t>(n), (st)))
+#else
+#define UP_IN(i, n, st) true
+#endif
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 

@@ -52,13 +52,15 @@ __global__ void slot_kernel(const int64_t* __restrict__ pos, const int32_t* __re
             const int mid = (lo + hi) >> 1;
             if (cu[mid] <= t) lo = mid; else hi = mid;
         }
+        if (!UP_IN(t, T_upper, status)) continue;
         const int64_t p = pos[t];
         const int64_t blk = p >= 0 ? p / B : -1;
         if (p < 0 || blk >= max_blocks || t >= cu[R]) {
             slots[t] = -1;
             set_status(status, UP_DEV_BAD_POSITION);
         } else {
-            slots[t] = static_cast<int64_t>(table[(int64_t)lo * max_blocks + blk]) * B + (p % B);
+            const int64_t e = (int64_t)lo * max_blocks + blk;
+            slots[t] = UP_IN(e, (int64_t)R * max_blocks, status) ? static_cast<int64_t>(table[e]) * B + (p % B) : -1;
         }
     }
 }
@@ -78,6 +80,8 @@ __global__ void seqused_kernel(const int32_t* __restrict__ kept_len, const uint8
     __syncthreads();
     const int prev = s_prev;
     for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
+        // up_seqused has no status word: an index outside kept_len is skipped, not reported
+        if (prev >= 0 && !UP_IN((int64_t)prev * R + r, (int64_t)L * R, nullptr)) continue;
         const int base = prev >= 0 ? kept_len[(int64_t)prev * R + r] : orig_len[r];
         seqused[r] = base + (kv_len[r] - orig_len[r]);
     }
@@ -132,6 +136,7 @@ extern "C" const char* up_status_string(int code, int device) {
             case UP_DEV_WAIT_TIMEOUT: return "a pipeline wait inside a kernel exceeded its time bound";
             case UP_DEV_BAD_POSITION: return "a position lies outside its block-table row";
             case UP_DEV_BAD_TOKEN_COUNT: return "num_actual_tokens lies outside [0, T_upper]";
+            case UP_DEV_BOUNDS: return "an index lies outside its array (bounds-checked build)";
             default: return "unknown device status";
         }
     }
@@ -149,6 +154,14 @@ extern "C" const char* up_status_string(int code, int device) {
 extern "C" uint64_t up_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
 
 extern "C" int up_abi_version(void) { return 2; }
+
+extern "C" int up_debug_bounds(void) {
+#ifdef UP_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 extern "C" size_t up_workspace_bytes(int R, int64_t T, int Hq, int Hkv, int dk, int G, int n, int64_t nb_cap) {
     const size_t a = up_score_workspace_bytes(R, T, Hq, Hkv, dk, G, n, nb_cap, 1);

@@ -82,6 +82,8 @@ struct Params {
     float* be;             // one pass: per (unit, key tile, block of the tile, row) block sums of 2^(S*a - m_t)
     float* bm;             // one pass: per (unit, key tile, row) the reference m_t of those sums
     int spt;               // one pass: blocks per key tile (128 / G)
+    // element counts of the workspace arrays (checked by the bounds-checked build)
+    int64_t lim_items, lim_units, lim_ml, lim_cvec, lim_blk, lim_tok, lim_be, lim_bm;
     float* block_scores;
     float* token_scores;
     int32_t* status;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
         if (blockIdx.x == 0) {
             for (int kk = 0; kk < P.units_per_req; ++kk) {
                 const int u = r * P.units_per_req + kk;
-                P.unit_items[u] = make_int2(off + kk * ni, ni);
+                if (UP_IN(u, P.lim_units, P.status)) P.unit_items[u] = make_int2(off + kk * ni, ni);
             }
         }
         if (in_smem) s_first[r] = off / NS;
@@ -276,7 +278,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
         const int kk = kq * NS + set;
         const int N = P.cu[r + 1] - P.cu[r];
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
-        P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
+        if (UP_IN(it, P.lim_items, P.status))
+            P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
     }
     if (tid == 0 && blockIdx.x == 0) {
         P.n_items[0] = total;
@@ -334,7 +337,7 @@ struct ItemInfo {
 __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 __device__ __forceinline__ ItemInfo item_info(const Params& P, int it) {
-    const int4 w = P.items[it];
+    const int4 w = UP_IN(it, P.lim_items, P.status) ? P.items[it] : make_int4(0, 0, 0, 0);
     ItemInfo I;
     I.r = uni(w.x);
     I.kk = uni(w.y);
@@ -805,7 +808,8 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
         if (PASS == 2 && I.unit != prev_unit) {
             named_bar_sync(1, kEpiThreads);
             for (int i = et; i < P.slab_rows; i += kEpiThreads)
-                S.cvec[i] = -__ldcg(P.cvec + (size_t)I.unit * P.slab_rows + i);
+                S.cvec[i] = UP_IN((int64_t)I.unit * P.slab_rows + i, P.lim_cvec, P.status)
+                                ? -__ldcg(P.cvec + (size_t)I.unit * P.slab_rows + i) : -INFINITY;
             named_bar_sync(1, kEpiThreads);
         }
         prev_unit = I.unit;
@@ -861,7 +865,8 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                 const float tot = (t01.x + t01.y) + (t23.x + t23.y);
                 const int i = kt * kTileKeys + rl;
                 const size_t part = (size_t)I.kk * 4 + wg;
-                if (P.tok != nullptr && i < I.N) P.tok[part * P.T + I.base + i] = tot;
+                if (P.tok != nullptr && i < I.N && UP_IN(part * P.T + I.base + i, P.lim_tok, P.status))
+                    P.tok[part * P.T + I.base + i] = tot;
                 const int nb = (I.N + P.G - 1) / P.G;
                 float* dst = P.blk + part * P.nb_cap + P.cb[I.r];
                 float s = tot;
@@ -869,7 +874,7 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                 for (int o = gw >> 1; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
                 if (P.G <= 32) {
                     const int g = i / P.G;
-                    if ((lane & (P.G - 1)) == 0 && g < nb) dst[g] = s;
+                    if ((lane & (P.G - 1)) == 0 && g < nb && UP_IN(dst + g - P.blk, P.lim_blk, P.status)) dst[g] = s;
                 } else {
                     float* wsum = reinterpret_cast<float*>(S.xchg) + (tile_par & 1) * 16 + wg * 4;
                     if (lane == 0) wsum[q] = s;
@@ -877,10 +882,11 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                     if (lane == 0) {
                         if (P.G == 64 && (q & 1) == 0) {
                             const int g = i / 64;
-                            if (g < nb) dst[g] = wsum[q] + wsum[q + 1];
+                            if (g < nb && UP_IN(dst + g - P.blk, P.lim_blk, P.status)) dst[g] = wsum[q] + wsum[q + 1];
                         } else if (P.G == 128 && q == 0) {
                             const int g = i / 128;
-                            if (g < nb) dst[g] = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
+                            if (g < nb && UP_IN(dst + g - P.blk, P.lim_blk, P.status))
+                                dst[g] = (wsum[0] + wsum[1]) + (wsum[2] + wsum[3]);
                         }
                     }
                 }
@@ -909,14 +915,16 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
                                 const float2 e = xm[(w2 * 2 + u) * 128 + rl];
                                 ll += e.y * ex2(e.x - mm);
                             }
-                        part[(size_t)(j * 128 + rl) * ui.y] = make_float2(mm, ll);
+                        if (UP_IN(part + (size_t)(j * 128 + rl) * ui.y - P.ml, P.lim_ml, P.status))
+                            part[(size_t)(j * 128 + rl) * ui.y] = make_float2(mm, ll);
                     }
                 }
                 named_bar_sync(1, kEpiThreads);
             } else {
                 int u = 0;
                 for (int j = jfirst; j < J; j += jstep, ++u)
-                    part[(size_t)(j * 128 + rl) * ui.y] = u ? make_float2(m1, l1) : make_float2(m0, l0);
+                    if (UP_IN(part + (size_t)(j * 128 + rl) * ui.y - P.ml, P.lim_ml, P.status))
+                        part[(size_t)(j * 128 + rl) * ui.y] = u ? make_float2(m1, l1) : make_float2(m0, l0);
             }
         }
     }
@@ -1046,12 +1054,13 @@ __device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_
             const bool masked = !__all_sync(0xffffffffu, lim >= kTileKeys - 1);
             one_pass_tile<CPB>(S, ta, wg, lane, masked, lim, a, m, l, e);
             const size_t t = tile0 + kt;
-            P.bm[t * P.slab_rows + row] = m;
+            if (UP_IN(t * P.slab_rows + row, P.lim_bm, P.status)) P.bm[t * P.slab_rows + row] = m;
             float* dst = P.be + t * SPT * P.slab_rows + row;
             float ts = 0.f;
 #pragma unroll
             for (int b = 0; b < SPT; ++b) {
-                dst[static_cast<size_t>(b) * P.slab_rows] = e[b];
+                if (UP_IN(dst + static_cast<size_t>(b) * P.slab_rows - P.be, P.lim_be, P.status))
+                    dst[static_cast<size_t>(b) * P.slab_rows] = e[b];
                 ts += e[b];
             }
             l += ts;
@@ -1059,7 +1068,7 @@ __device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_
         // this item's (m, l) partial of the row, merged over the 4 / J warpgroups that hold the row
         float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;
         if (J == 4) {
-            part[(size_t)row * ui.y] = make_float2(m, l);
+            if (UP_IN(part + (size_t)row * ui.y - P.ml, P.lim_ml, P.status)) part[(size_t)row * ui.y] = make_float2(m, l);
         } else {
             float2* xm = reinterpret_cast<float2*>(S.xchg);                  // [4 warpgroups][128 rows]
             xm[wg * 128 + rl] = make_float2(m, l);
@@ -1073,7 +1082,7 @@ __device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_
                         const float2 x = xm[w2 * 128 + rl];
                         ll += x.y * ex2(x.x - mm);
                     }
-                part[(size_t)row * ui.y] = make_float2(mm, ll);
+                if (UP_IN(part + (size_t)row * ui.y - P.ml, P.lim_ml, P.status)) part[(size_t)row * ui.y] = make_float2(mm, ll);
             }
             named_bar_sync(1, kEpiThreads);
         }
@@ -1093,6 +1102,7 @@ __global__ void __launch_bounds__(256) merge_kernel(Params P) {
         const int u = static_cast<int>(gr / P.slab_rows), row = static_cast<int>(gr % P.slab_rows);
         const int2 ui = P.unit_items[u];
         const float2* part = P.ml + (size_t)ui.x * P.slab_rows + (size_t)row * ui.y;
+        if (!UP_IN(u, P.lim_units, P.status) || !UP_IN(part + ui.y - 1 - P.ml, P.lim_ml, P.status)) continue;
         // the first kCache partials of each lane stay in registers between the max and the sum (one
         // round of loads instead of two); the sum keeps its order (p = lane, lane + 32, ...)
         constexpr int kCache = 8;
@@ -1119,7 +1129,8 @@ __global__ void __launch_bounds__(256) merge_kernel(Params P) {
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) ll += __shfl_xor_sync(0xffffffffu, ll, o);
-        if (lane == 0) P.cvec[(size_t)u * P.slab_rows + row] = mm == -INFINITY ? INFINITY : mm + log2f(ll);
+        if (lane == 0 && UP_IN((size_t)u * P.slab_rows + row, P.lim_cvec, P.status))
+            P.cvec[(size_t)u * P.slab_rows + row] = mm == -INFINITY ? INFINITY : mm + log2f(ll);
     }
 }
 
@@ -1245,12 +1256,14 @@ __global__ void finalize_kernel(Params P) {
     for (int gb = blockIdx.x * blockDim.x + threadIdx.x; gb < nb_total; gb += stride) {
         const int r = find_segment(P.cb, P.R, gb);
         const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
+        if (!UP_IN(gb + (int64_t)(parts - 1) * P.nb_cap, P.lim_blk, P.status) || !UP_IN(gb, P.nb_cap, P.status)) continue;
         P.block_scores[gb] = sum_parts(P.blk + gb, P.nb_cap, parts) * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
     }
     if (P.token_scores != nullptr) {
         for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < P.T; t += stride) {
             const int r = find_segment(P.cu, P.R, t);
             const int ne = min(P.n, P.cu[r + 1] - P.cu[r]);
+            if (!UP_IN(t + (int64_t)(parts - 1) * P.T, P.lim_tok, P.status)) continue;
             P.token_scores[t] = sum_parts(P.tok + t, P.T, parts) * (1.0f / (static_cast<float>(ne) * P.Hq));
         }
     }
@@ -1314,6 +1327,14 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
                 if (i < pairs) {
                     const int kk = i / rows4, r0 = (i - kk * rows4) * 4;
                     const size_t t = static_cast<size_t>(s_tile0[kk]) + tile;
+                    if (!UP_IN(t * rows + r0 + 3, P.lim_bm, P.status) ||
+                        !UP_IN((t * SPT + SPT - 1) * rows + r0 + 3, P.lim_be, P.status) ||
+                        !UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status)) {
+                        wv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                        for (int s = 0; s < SPT; ++s) ev[b][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        continue;
+                    }
                     const float4 m4 = ldcg4(P.bm + t * rows + r0);
                     const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
 #pragma unroll
@@ -1345,7 +1366,8 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
                 float x = 0.f;
                 for (int w2 = 0; w2 < kReduceThreads / 32; ++w2) x += s_part[w2][threadIdx.x];
                 const int ne = min(P.n, N);
-                P.block_scores[P.cb[r] + g] = x * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
+                if (UP_IN(P.cb[r] + g, P.nb_cap, P.status))
+                    P.block_scores[P.cb[r] + g] = x * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
             }
         }
         __syncthreads();
@@ -1507,6 +1529,14 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.be = one_pass ? reinterpret_cast<float*>(w + L.be) : nullptr;
     P.bm = one_pass ? reinterpret_cast<float*>(w + L.bm) : nullptr;
     P.spt = kTileKeys / G;
+    P.lim_items = L.items_cap;
+    P.lim_units = L.units;
+    P.lim_ml = L.items_cap * g.slab_rows;
+    P.lim_cvec = L.units * g.slab_rows;
+    P.lim_blk = static_cast<int64_t>(Hkv) * g.slabs * 4 * nb_cap;
+    P.lim_tok = token_scores ? static_cast<int64_t>(Hkv) * g.slabs * 4 * T : 0;
+    P.lim_be = one_pass ? L.items_cap * kItemTiles * (kTileKeys / G) * g.slab_rows : 0;
+    P.lim_bm = one_pass ? L.items_cap * kItemTiles * g.slab_rows : 0;
     P.block_scores = block_scores;
     P.token_scores = token_scores;
     P.status = dev_status;

@@ -69,19 +69,22 @@ __device__ __forceinline__ T block_exclusive_scan(T v, T* sh, T* total) {
 // (i >= N - n); the aligned interior is written 16 bytes per store (token_keep is 16-byte aligned), the
 // unaligned head and tail byte by byte.
 template <typename RankedFn>
-__device__ __forceinline__ void write_token_mask(uint8_t* token_keep, int c0, int N, int G, int A, int n,
-                                                 RankedFn ranked) {
+__device__ __forceinline__ void write_token_mask(uint8_t* token_keep, int T, int c0, int N, int G, int A, int n,
+                                                 RankedFn ranked, int32_t* status) {
     const int tid = threadIdx.x;
     const int gshift = __ffs(G) - 1;
     auto keep_byte = [&](int i) -> uint32_t { return (ranked(i >> gshift) || i < A || i >= N - n) ? 1u : 0u; };
     const int64_t a0 = c0, a1 = (int64_t)c0 + N;
     const int64_t v0 = min((a0 + 15) & ~int64_t(15), a1), v1 = max(a1 & ~int64_t(15), v0);
-    for (int64_t t = a0 + tid; t < v0; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
-    for (int64_t t = v1 + tid; t < a1; t += kThreads) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    for (int64_t t = a0 + tid; t < v0; t += kThreads)
+        if (UP_IN(t, T, status)) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
+    for (int64_t t = v1 + tid; t < a1; t += kThreads)
+        if (UP_IN(t, T, status)) token_keep[t] = static_cast<uint8_t>(keep_byte(static_cast<int>(t - a0)));
     // with the request start 16-byte aligned and G >= 16, a 16-byte group lies in one block; clear
     // of the sinks and the window it is that block's flag repeated
     const bool whole = G >= 16 && v0 == a0;
     for (int64_t t = v0 + 16 * (int64_t)tid; t < v1; t += 16 * (int64_t)kThreads) {
+        if (!UP_IN(t + 15, T, status)) continue;
         const int i0 = static_cast<int>(t - a0);
         if (whole && i0 >= A && i0 + 15 < N - n) {
             const uint32_t b = ranked(i0 >> gshift) ? 0x01010101u : 0u;
@@ -106,8 +109,8 @@ __device__ __forceinline__ void write_token_mask(uint8_t* token_keep, int c0, in
 // block_keep, from which the token mask is written; the forced blocks are set last.
 __device__ __noinline__ void select_large(const float* __restrict__ bs, int b0, int nb, int64_t nb_cap, int c0, int N,
                                           int G, int n, int A, double p, uint64_t* ws_keys, uint8_t* block_keep,
-                                          uint8_t* token_keep, int32_t* kstar, int r, uint8_t* sm, double* shd,
-                                          int* shi, double* s_total, int* s_below) {
+                                          uint8_t* token_keep, int32_t* kstar, int r, int T, uint8_t* sm,
+                                          double* shd, int* shi, double* s_total, int* s_below, int32_t* status) {
     constexpr int kTileKeys = kThreads * kMaxIpt;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     uint64_t* src = ws_keys + b0;
@@ -116,7 +119,8 @@ __device__ __noinline__ void select_large(const float* __restrict__ bs, int b0, 
     uint32_t* dbase = hist + kRadix * kWarps;                           // [kRadix] next destination of a digit
     for (int k = tid; k < nb; k += kThreads) {                          // position k holds block nb - 1 - k
         const int g = nb - 1 - k;
-        src[k] = pack_key(bs[b0 + g], static_cast<uint32_t>(g));
+        if (UP_IN(b0 + k, nb_cap, status) && UP_IN(b0 + g, nb_cap, status))
+            src[k] = pack_key(bs[b0 + g], static_cast<uint32_t>(g));
     }
     __syncthreads();
     const uint32_t lt_mask = (1u << lane) - 1u;
@@ -162,7 +166,8 @@ __device__ __noinline__ void select_large(const float* __restrict__ bs, int b0, 
             __syncthreads();
 #pragma unroll
             for (int j = 0; j < kMaxIpt; ++j)
-                if (dig[j] < 0x100u) dst[hist[dig[j] * kWarps + warp] + rank[j]] = src[base_k + 32 * j];
+                if (dig[j] < 0x100u && UP_IN(hist[dig[j] * kWarps + warp] + rank[j], nb, status))
+                    dst[hist[dig[j] * kWarps + warp] + rank[j]] = src[base_k + 32 * j];
             __syncthreads();
         }
         uint64_t* t = src;
@@ -208,13 +213,16 @@ __device__ __noinline__ void select_large(const float* __restrict__ bs, int b0, 
     if (below) atomicAdd(s_below, below);
     __syncthreads();
     const int ks = min(nb, *s_below + 1);
-    for (int k = tid; k < nb; k += kThreads) block_keep[b0 + static_cast<uint32_t>(src[k])] = k < ks ? 1 : 0;
+    for (int k = tid; k < nb; k += kThreads) {
+        const uint32_t g = static_cast<uint32_t>(src[k]);
+        if (UP_IN(g, nb, status)) block_keep[b0 + g] = k < ks ? 1 : 0;
+    }
     __syncthreads();
-    write_token_mask(token_keep, c0, N, G, A, n, [&](int g) { return block_keep[b0 + g] != 0; });
+    write_token_mask(token_keep, T, c0, N, G, A, n, [&](int g) { return block_keep[b0 + g] != 0; }, status);
     __syncthreads();
     for (int g = tid; g < nb; g += kThreads) {
         const bool forced = (static_cast<int64_t>(g) * G < A) || (static_cast<int64_t>(g + 1) * G > static_cast<int64_t>(N) - n);
-        if (forced) block_keep[b0 + g] = 1;
+        if (forced && UP_IN(b0 + g, nb_cap, status)) block_keep[b0 + g] = 1;
     }
     if (tid == 0) kstar[r] = ks;
 }
@@ -257,8 +265,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     }
     const int b0 = cb[r];
     if (nb > UP_MAX_BLOCKS_PER_REQUEST) {
-        select_large(bs, b0, nb, nb_cap, c0, N, G, n, A, p, ws_keys, block_keep, token_keep, kstar, r, sm, shd, shi,
-                     &s_total, &s_below);
+        select_large(bs, b0, nb, nb_cap, c0, N, G, n, A, p, ws_keys, block_keep, token_keep, kstar, r, T, sm, shd,
+                     shi, &s_total, &s_below, status);
         return;
     }
     const int ipt = (nb + kThreads - 1) / kThreads;      // keys per thread
@@ -267,7 +275,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     // 1. packed keys, position k holds block g = nb-1-k (padding slots get key 0, which sorts last)
     for (int k = tid; k < npad; k += kThreads) {
         const int g = nb - 1 - k;
-        keys[k] = g >= 0 ? pack_key(bs[b0 + g], static_cast<uint32_t>(g)) : 0ull;
+        keys[k] = g >= 0 && UP_IN(b0 + g, nb_cap, status) ? pack_key(bs[b0 + g], static_cast<uint32_t>(g)) : 0ull;
     }
     __syncthreads();
 
@@ -386,14 +394,15 @@ __global__ void __launch_bounds__(kThreads) select_kernel(const float* __restric
     // 4. ranked flags by block index, then block and token masks
     for (int j = 0; j < ipt; ++j) {
         const int k = k0 + j;
-        if (k < nb) ranked[static_cast<uint32_t>(keys[k])] = k < ks;
+        if (k < nb && UP_IN(static_cast<uint32_t>(keys[k]), UP_MAX_BLOCKS_PER_REQUEST, status))
+            ranked[static_cast<uint32_t>(keys[k])] = k < ks;
     }
     __syncthreads();
     for (int g = tid; g < nb; g += kThreads) {
         const bool forced = (static_cast<int64_t>(g) * G < A) || (static_cast<int64_t>(g + 1) * G > static_cast<int64_t>(N) - n);
-        block_keep[b0 + g] = (ranked[g] || forced) ? 1 : 0;
+        if (UP_IN(b0 + g, nb_cap, status)) block_keep[b0 + g] = (ranked[g] || forced) ? 1 : 0;
     }
-    write_token_mask(token_keep, c0, N, G, A, n, [&](int g) { return ranked[g] != 0; });
+    write_token_mask(token_keep, T, c0, N, G, A, n, [&](int g) { return ranked[g] != 0; }, status);
     if (tid == 0) kstar[r] = ks;
 }
 

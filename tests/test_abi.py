@@ -38,6 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 def test_sizing_helpers(lib):
     import long_context_prefill_varlen_gb300 as up
     assert up.up_abi_version() == 2
+    assert up.up_debug_bounds() == 0               # the normal build; libuniprefill_debug.so returns 1
     assert up.up_max_blocks(3, 1000, 64) == 1000 // 64 + 3
     nb = up.up_max_blocks(1, 32768, 64)
     a = up.up_score_workspace_bytes(1, 32768, 32, 8, 128, 64, 128, nb)
