@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--p", type=float, default=None, help="override the workload's top-p threshold")
+    ap.add_argument("--requests", type=int, default=None,
+                    help="keep only the workload's first K requests (a smaller case of the same geometry)")
     ap.add_argument("--sweep", choices=["rho", "ablation", "stack"], default=None,
                     help="instead of the step line, one JSON line per point: 'rho' = compaction and scatter "
                          "bandwidth against the kept fraction; 'ablation' = the step's stages over G, n and p; "
@@ -599,6 +601,9 @@ def main():
     w = recipe.workload(args.config)
     if args.p is not None:
         w = w.replace(p=args.p)
+    if args.requests is not None and args.requests < w.R:
+        k = max(1, args.requests)
+        w = w.replace(lengths=w.lengths[:k], name=f"{w.name}; its first {k} request(s) only")
     if args.sweep is not None:
         if rank == 0:
             run_sweep(args, w)
