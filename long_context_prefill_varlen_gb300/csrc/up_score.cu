@@ -582,6 +582,31 @@ __device__ __forceinline__ void tmem_wait_pin(uint32_t (&v)[16]) {
                    "+r"(v[15]));
 }
 
+// 32 consecutive fp32 columns of this warp's 32 TMEM lanes, without waiting
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_wait_pin32(uint32_t (&v)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]));
+    asm volatile(""
+                 : "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]), "+r"(v[22]),
+                   "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]), "+r"(v[29]),
+                   "+r"(v[30]), "+r"(v[31]));
+}
+
 __device__ __forceinline__ float f(uint32_t x) { return __uint_as_float(x); }
 
 // Packed fp32 pairs: the f32x2 forms of add and fma do the work of two scalar instructions in one
@@ -943,38 +968,6 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
 // sums (G times smaller than S) instead of over a recomputed S: the tensor work and the exponentials of
 // the recompute pass disappear; S itself is never stored.
 
-// one 16-column chunk of this thread's row in the one pass: fold its maximum into m (rescaling the block
-// sums of the tile so far and the l of the item's earlier tiles when it grows), then add the sum of
-// 2^(S*a - m) over the chunk to its block's sum e[ch / CPB] (CPB = G / 16 chunks per block).  Columns
-// outside the causal range arrive as -inf and add 0.
-template <int CPB>
-__device__ __forceinline__ void one_pass_chunk(const uint32_t (&v)[16], int ch, float a, float& m, float& l,
-                                               float (&e)[8 / CPB]) {
-    const float x0 = max3(f(v[0]), f(v[1]), f(v[2])), x1 = max3(f(v[3]), f(v[4]), f(v[5]));
-    const float x2 = max3(f(v[6]), f(v[7]), f(v[8])), x3 = max3(f(v[9]), f(v[10]), f(v[11]));
-    const float x4 = max3(f(v[12]), f(v[13]), f(v[14]));
-    const float mx = max3(max3(x0, x1, x2), max3(x3, x4, f(v[15])), x0) * a;
-    if (mx > m) {
-        const float sc = ex2(m - mx);           // 0 while m = -inf
-        l *= sc;
-#pragma unroll
-        for (int b = 0; b < 8 / CPB; ++b)
-            if (b <= ch / CPB) e[b] *= sc;
-        m = mx;
-    }
-    // while m is -inf every value so far is -inf: any finite reference gives the sum 0, not NaN
-    const float mr = m == -INFINITY ? 0.f : m;
-    const uint64_t a2 = pk2(a, a), nm2 = pk2(-mr, -mr);
-    uint64_t s0 = p2(v, 0, a2, nm2), s1 = p2(v, 2, a2, nm2);
-#pragma unroll
-    for (int c = 4; c < 16; c += 4) {
-        s0 = add2(s0, p2(v, c, a2, nm2));
-        s1 = add2(s1, p2(v, c + 2, a2, nm2));
-    }
-    const float2 t = up2(add2(s0, s1));
-    e[ch / CPB] += t.x + t.y;
-}
-
 // columns 16*ch + c > lim of a chunk become -inf (keys after the row's position, or a row that is not a
 // window row of this request: lim < 0)
 __device__ __forceinline__ void mask_chunk(uint32_t (&v)[16], int ch, int lim) {
@@ -983,25 +976,75 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&v)[16], int ch, int lim) {
         if (16 * ch + c > lim) v[c] = 0xFF800000u;
 }
 
-// one whole 128-column job of this thread's row: eight chunks, TMEM loads double-buffered, the buffer
-// released as soon as its last chunk has landed; `masked` (warp-uniform) applies the causal limit lim
+// 32 columns (the 16-column chunks 2*h2 and 2*h2+1) of this thread's row in the one pass: fold their
+// maximum into m (rescaling the block sums of the tile so far and the l of the item's earlier tiles when
+// it grows), then add 2^(S*a - m) over each chunk to its block's sum e[chunk / CPB] (CPB = G / 16 chunks
+// per block).  One maximum update per 32 columns leaves 32 independent exponentials behind it (measured
+// 2-8% faster score calls than an update per 16 columns).  Columns outside the causal range arrive as
+// -inf and add 0.
+template <int CPB>
+__device__ __forceinline__ void one_pass_chunk32(const uint32_t (&v)[32], int h2, float a, float& m, float& l,
+                                                 float (&e)[8 / CPB]) {
+    float x[6];
+#pragma unroll
+    for (int i = 0; i < 5; ++i) x[i] = max3(f(v[6 * i]), f(v[6 * i + 1]), f(v[6 * i + 2]));
+    x[5] = max3(f(v[3]), f(v[4]), f(v[5]));
+    float y0 = max3(f(v[9]), f(v[10]), f(v[11])), y1 = max3(f(v[15]), f(v[16]), f(v[17]));
+    float y2 = max3(f(v[21]), f(v[22]), f(v[23])), y3 = max3(f(v[27]), f(v[28]), f(v[29]));
+    const float z = max3(f(v[30]), f(v[31]), x[0]);
+    const float mx = max3(max3(x[1], x[2], x[3]), max3(x[4], x[5], z), max3(y0, y1, max(y2, y3))) * a;
+    if (mx > m) {
+        const float sc = ex2(m - mx);           // 0 while m = -inf
+        l *= sc;
+#pragma unroll
+        for (int b = 0; b < 8 / CPB; ++b)
+            if (b <= (2 * h2 + 1) / CPB) e[b] *= sc;
+        m = mx;
+    }
+    // while m is -inf every value so far is -inf: any finite reference gives the sum 0, not NaN
+    const float mr = m == -INFINITY ? 0.f : m;
+    const uint64_t a2 = pk2(a, a), nm2 = pk2(-mr, -mr);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t(&w)[16] = *reinterpret_cast<const uint32_t(*)[16]>(&v[16 * hf]);
+        uint64_t s0 = p2(w, 0, a2, nm2), s1 = p2(w, 2, a2, nm2);
+#pragma unroll
+        for (int c = 4; c < 16; c += 4) {
+            s0 = add2(s0, p2(w, c, a2, nm2));
+            s1 = add2(s1, p2(w, c + 2, a2, nm2));
+        }
+        const float2 t = up2(add2(s0, s1));
+        e[(2 * h2 + hf) / CPB] += t.x + t.y;
+    }
+}
+
+// one whole 128-column job of this thread's row, the buffer released as soon as its last columns have
+// landed; `masked` (warp-uniform) applies the causal limit lim
 template <int CPB>
 __device__ __forceinline__ void one_pass_tile(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool masked, int lim,
                                               float a, float& m, float& l, float (&e)[8 / CPB]) {
-    uint32_t va[16], vb[16];
-    tmem_ld16(ta, va);
-    tmem_wait_pin(va);
+    // 32-column loads, double-buffered: the load of the next 32 columns is in flight while the current
+    // 32 are reduced with one maximum update
+    uint32_t va[32], vb[32];
+    tmem_ld32(ta, va);
+    tmem_wait_pin32(va);
 #pragma unroll
-    for (int ch = 0; ch < 8; ch += 2) {
-        tmem_ld16(ta + (ch + 1) * 16, vb);
-        if (masked) mask_chunk(va, ch, lim);
-        one_pass_chunk<CPB>(va, ch, a, m, l, e);
-        tmem_wait_pin(vb);
-        if (ch + 2 < 8) tmem_ld16(ta + (ch + 2) * 16, va);
+    for (int h = 0; h < 4; h += 2) {
+        tmem_ld32(ta + (h + 1) * 32, vb);
+        if (masked) {
+            mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[0]), 2 * h, lim);
+            mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[16]), 2 * h + 1, lim);
+        }
+        one_pass_chunk32<CPB>(va, h, a, m, l, e);
+        tmem_wait_pin32(vb);
+        if (h + 2 < 4) tmem_ld32(ta + (h + 2) * 32, va);
         else release_tmem(S, buf, lane);
-        if (masked) mask_chunk(vb, ch + 1, lim);
-        one_pass_chunk<CPB>(vb, ch + 1, a, m, l, e);
-        if (ch + 2 < 8) tmem_wait_pin(va);
+        if (masked) {
+            mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[0]), 2 * h + 2, lim);
+            mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[16]), 2 * h + 3, lim);
+        }
+        one_pass_chunk32<CPB>(vb, h + 1, a, m, l, e);
+        if (h + 2 < 4) tmem_wait_pin32(va);
     }
 }
 
