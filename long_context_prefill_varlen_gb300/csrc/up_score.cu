@@ -14,10 +14,11 @@
 //   final   b_g = (sum over units of the partials) / (n_eff * Hq * G).
 // a = sm_scale * log2(e): the softmax is computed in base 2, exactly equal to exp in base e.
 //
-// CTA layout (608 threads, one CTA per SM, persistent over a contiguous range of work items):
+// CTA layout (640 threads, one CTA per SM, persistent over a contiguous range of work items):
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warp 1     TMEM allocator and tcgen05.mma issuer of the even jobs; warp 18 issues the odd jobs
-//              (all three run their loop on the whole warp and issue from one elected lane)
+//   warp 1     TMEM allocator and tcgen05.mma issuer of the jobs in TMEM buffers 0 and 3; warps 18
+//              and 19 issue those in buffers 1 and 2 (these warps run their loop on the whole warp
+//              and issue from one elected lane)
 //   warps 2-17 four epilogue warpgroups.  A job is one 128 x W fp32 accumulator (W = 128 query rows;
 //              W = 256 in pass 2 when the slab has 256 rows); with J jobs per key tile,
 //              warpgroup g takes jobs g, g+4, ... when J >= 3, half a job when J = 2 and a quarter
@@ -42,7 +43,7 @@ constexpr int kStages = 5;
 constexpr int kSlabBytes = 128 * 1024;          // resident query rows of one unit
 constexpr int kItemTiles = 2;                   // key tiles per work item (pass-1 partial granularity)
 constexpr int kEpiThreads = 512;
-constexpr int kIssuers = 2;                     // MMA issuer warps (warps 1 and 18), jobs split by parity
+constexpr int kIssuers = 3;                     // MMA issuer warps (warps 1, 18 and 19); see mma_issuer
 constexpr int kEpiWarp0 = 2;                    // epilogue warps 2..17
 constexpr int kIssuer1Warp = kEpiWarp0 + kEpiThreads / 32;
 constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
@@ -424,14 +425,16 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
 // the advance is a plain add on the descriptor.
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Two issuer warps share the jobs by parity of the running job count: warp w issues job q iff
-// (q & 1) == w.  A tcgen05.commit holds up the thread that issues it until its earlier MMAs have
-// drained, and a single issuer that commits once per job leaves the tensor pipe idle for that
-// time (measured: 128x128x16 MMAs at ~96 instead of 64 cycles); with two issuers one warp's
-// commit overlaps the other's MMAs.  A commit tracks only its own thread's MMAs, so every barrier
+// Three issuer warps share the jobs by TMEM buffer: issuer w issues the jobs whose buffer b has
+// b mod 3 == w.  A tcgen05.commit holds up the thread that issues it until its earlier MMAs have
+// drained, so an issuer keeps one job in flight, and around each job it spends a few hundred cycles
+// in the commit, the buffer wait and its loop (cycle-stamped timelines); several issuers keep several
+// jobs in flight.  A commit tracks only its own thread's MMAs, so every barrier
 // that releases an operand (K stage, query slab) takes one commit from each issuer, and each
 // issuer waits for a stage to land before it commits the stage's release, even when it issued no
 // job on that tile: its arrival can then never count toward a later use of the stage.
+static_assert(kThreads == 640 && kIssuer1Warp + kIssuers - 2 == kThreads / 32 - 1,
+              "warps: producer 0, issuers 1, 18 and 19, epilogue 2-17");
 template <int PASS, int NC>
 __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1, uint32_t w) {
     volatile int* abort_flag = S.abort_flag;
@@ -454,7 +457,11 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
         if (leader) tc_commit(bar);
         __syncwarp();
     };
-    auto mine = [&](uint32_t q) { return (q & 1u) == w; };
+    // every use of a TMEM buffer is issued by the same warp (buffer b by issuer b mod kIssuers): its waits
+    // for the buffer then always refer to the phase just before the current one, whatever the other
+    // issuers do (with jobs handed out round-robin an issuer could run two uses ahead on a buffer and
+    // read its parity from the wrong phase)
+    auto mine = [&](uint32_t q) { return (q & (jm.nbuf - 1)) % kIssuers == w; };
     for (int it = it0; it < it1; ++it) {
         const ItemInfo I = item_info(P, it);
         if (I.unit != prev_unit) {
@@ -1234,8 +1241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         producer<NC>(P, S, &tmQ, &tmK, it0, it1);
-    } else if (warp == 1 || warp == kIssuer1Warp) {
-        mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : 1u);
+    } else if (warp == 1 || warp >= kIssuer1Warp) {
+        // warps 1, 18 and 19 (kThreads covers exactly these and the producer and epilogue warps)
+        mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : static_cast<uint32_t>(warp - kIssuer1Warp + 1));
     } else if (PASS == 3) {
         switch (P.spt) {                         // blocks per key tile = 128 / G
             case 8: epilogue_one_pass<1>(P, S, tmem_base, it0, it1); break;
