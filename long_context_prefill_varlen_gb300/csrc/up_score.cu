@@ -147,7 +147,7 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
     L.units = (int64_t)R * Hkv * g.slabs;
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
-    L.items = take(sizeof(int4) * L.items_cap);
+    L.items = take(sizeof(int4) * 2 * L.items_cap);      // two entries per item (see item_decode)
     L.unit_items = take(sizeof(int2) * L.units);
     L.n_items = take(16);
     L.ml = take(sizeof(float2) * L.items_cap * g.slab_rows);
@@ -279,8 +279,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
         const int kk = kq * NS + set;
         const int N = P.cu[r + 1] - P.cu[r];
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
-        if (UP_IN(it, P.lim_items, P.status))
-            P.items[it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
+        if (UP_IN(it, P.lim_items, P.status)) {
+            P.items[2 * it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
+            P.items[2 * it + 1] = make_int4(P.cu[r], N, 0, 0);
+        }
     }
     if (tid == 0 && blockIdx.x == 0) {
         P.n_items[0] = total;
@@ -337,16 +339,26 @@ struct ItemInfo {
 // computed from the schedule below stays in warp-uniform registers (every caller is a full warp).
 __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
-__device__ __forceinline__ ItemInfo item_info(const Params& P, int it) {
-    const int4 w = UP_IN(it, P.lim_items, P.status) ? P.items[it] : make_int4(0, 0, 0, 0);
+// An item is two entries of the list: (request, unit of the request, first tile, end tile) and (the
+// request's first token, its length), loaded together (no dependent loads).  The producer and the MMA
+// issuers, which set the pace, load the next item's entries while they work on the current one.
+__device__ __forceinline__ void item_load(const Params& P, int it, int it1, int4& a, int4& b) {
+    if (it < it1 && UP_IN(it, P.lim_items, P.status)) {
+        a = P.items[2 * it];
+        b = P.items[2 * it + 1];
+    } else {
+        a = b = make_int4(0, 0, 0, 0);
+    }
+}
+__device__ __forceinline__ ItemInfo item_decode(const Params& P, const int4& a, const int4& b) {
     ItemInfo I;
-    I.r = uni(w.x);
-    I.kk = uni(w.y);
-    I.tb = uni(w.z);
-    I.te = uni(w.w);
+    I.r = uni(a.x);
+    I.kk = uni(a.y);
+    I.tb = uni(a.z);
+    I.te = uni(a.w);
     I.unit = I.r * P.units_per_req + I.kk;
-    I.base = uni(P.cu[I.r]);
-    I.N = uni(P.cu[I.r + 1]) - I.base;
+    I.base = uni(b.x);
+    I.N = uni(b.y);
     I.kh = I.kk / P.slabs;
     I.slab = I.kk % P.slabs;
     return I;
@@ -374,8 +386,11 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
     uint32_t stage_cnt = 0, slab_cnt = 0;
     const uint32_t slab_addr = smem_u32(S.slab), stage_addr = smem_u32(S.stages);
     const bool leader = elect_one();
+    int4 na, nb;
+    item_load(P, it0, it1, na, nb);
     for (int it = it0; it < it1; ++it) {
-        const ItemInfo I = item_info(P, it);
+        const ItemInfo I = item_decode(P, na, nb);
+        item_load(P, it + 1, it1, na, nb);
         if (I.unit != prev_unit) {
             if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(S.slab_free), (slab_cnt & 1) ^ 1, abort_flag))) {
                 if (leader) drain_loads(S, stage_cnt, slab_cnt);
@@ -462,8 +477,11 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
     // issuers do (with jobs handed out round-robin an issuer could run two uses ahead on a buffer and
     // read its parity from the wrong phase)
     auto mine = [&](uint32_t q) { return (q & (jm.nbuf - 1)) % kIssuers == w; };
+    int4 na, nb;
+    item_load(P, it0, it1, na, nb);
     for (int it = it0; it < it1; ++it) {
-        const ItemInfo I = item_info(P, it);
+        const ItemInfo I = item_decode(P, na, nb);
+        item_load(P, it + 1, it1, na, nb);
         if (I.unit != prev_unit) {
             if (prev_unit >= 0) commit(smem_u32(S.slab_free));
             if (!wait_all(smem_u32(S.slab_full), slab_cnt & 1)) goto out;
@@ -834,7 +852,9 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
     int rmod0 = 0, rmod1 = 0;
 
     for (int it = it0; it < it1; ++it) {
-        const ItemInfo I = item_info(P, it);
+        int4 ia, ib;
+        item_load(P, it, it1, ia, ib);
+        const ItemInfo I = item_decode(P, ia, ib);
         const int ne = min(P.n, I.N);
         const int row0 = I.slab * P.slab_rows;   // first global query row of this slab
         if (PASS == 2 && I.unit != prev_unit) {
@@ -1076,7 +1096,9 @@ __device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_
     bool rin = false;
     int rmod = 0;
     for (int it = it0; it < it1; ++it) {
-        const ItemInfo I = item_info(P, it);
+        int4 ia, ib;
+        item_load(P, it, it1, ia, ib);
+        const ItemInfo I = item_decode(P, ia, ib);
         if (I.slab != prev_slab) {
             const int qg = I.slab * P.slab_rows + row;
             rin = qg < P.rows_total;
