@@ -2,28 +2,30 @@
 // Prefill Acceleration via Block-wise Dynamic Sparsification", arXiv 2605.06221, section 3.2,
 // Eqs. 2-4, and the kernel pipeline of section 3.5, Eq. 13).
 //
-// For every request r, KV head kh and the group x n window query rows that read kh:
-//   pass 1  S = Qwin . K^T on tcgen05 (query rows in TMEM lanes, 128 keys per tile in columns);
-//           per row the online max m and sum l of 2^(S*a - m) over the causal key range;
-//           per work item (kItemTiles key tiles) a partial (m, l).
-//   merge   per query row, the partials of its (r, kh, slab) unit folded in a fixed order into
-//           c = m + log2(l) (one warp per row).
-//   pass 2  S^T = K . Qwin^T (128 keys in TMEM lanes, query rows in columns); each thread owns a
-//           key and sums P = 2^(S*a - c_row) over its rows; the per-key sums are reduced over G
-//           consecutive keys with warp shuffles and written as per-(unit, block) partials.
-//   final   b_g = (sum over units of the partials) / (n_eff * Hq * G).
+// For every request r, KV head kh and the group x n window query rows that read kh, S = Qwin . K^T
+// is computed on tcgen05 (query rows in TMEM lanes, 128 keys per tile in columns) in one of two ways.
+//   one pass (the default)  per row the online max m and sum l of 2^(S*a - m) over the causal key
+//           range, per work item (kItemTiles key tiles) a partial (m, l), and per key tile the sums of
+//           2^(S*a - m_t) over each block with their reference maxima m_t; the merge kernel folds the
+//           partials into c = m + log2(l) per row, and the reduce kernel forms b_g from the block sums
+//           scaled by 2^(m_t - c) (see the one-pass section).  S is computed once and never stored.
+//   two passes (when per-token scores are asked for)  pass 1 as above without the block sums, the
+//           merge, then pass 2 recomputes S^T = K . Qwin^T (keys in TMEM lanes) and sums
+//           P = 2^(S*a - c_row) per key over its rows, reduced over G keys with warp shuffles into
+//           per-(unit, block) partials; the final kernel divides by n_eff * Hq * G.
 // a = sm_scale * log2(e): the softmax is computed in base 2, exactly equal to exp in base e.
 //
 // CTA layout (640 threads, one CTA per SM, persistent over a contiguous range of work items):
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warp 1     TMEM allocator and tcgen05.mma issuer of the jobs in TMEM buffers 0 and 3; warps 18
-//              and 19 issue those in buffers 1 and 2 (these warps run their loop on the whole warp
-//              and issue from one elected lane)
+//   warps 1, 18, 19  tcgen05.mma issuers (warp 1 also allocates TMEM; each runs its loop on the whole
+//              warp and issues from one elected lane), see mma_issuer
 //   warps 2-17 four epilogue warpgroups.  A job is one 128 x W fp32 accumulator (W = 128 query rows;
-//              W = 256 in pass 2 when the slab has 256 rows); with J jobs per key tile,
-//              warpgroup g takes jobs g, g+4, ... when J >= 3, half a job when J = 2 and a quarter
-//              when J = 1.  TMEM is read in 16-column chunks, the next chunk's load in flight while
-//              the current one is reduced.
+//              W = 256 in pass 2 when the slab has 256 rows).  One pass: warpgroup w drains TMEM
+//              buffer w whole at d_k <= 128, and at d_k = 256 the pairs of warpgroups drain alternate
+//              buffers, 64 columns each.  Two passes: with J jobs per key tile warpgroup g takes jobs
+//              g, g+4, ... when J >= 3, half a job when J = 2 and a quarter when J = 1.  TMEM is read
+//              in 16- or 32-column chunks, the next chunk's load in flight while the current one is
+//              reduced.
 // TMEM: the whole 512 columns, a ring of 4 (W = 128) or 2 (W = 256) accumulators.
 // Per element the epilogue spends one ex2 on the SFU (32/clk/SM on this part, the same rate at
 // which the tensor core produces S elements at d_k = 128) plus one FFMA and one FADD.
@@ -80,8 +82,8 @@ struct Params {
     float* cvec;
     float* blk;
     float* tok;
-    float* be;             // one pass: per (unit, key tile, block of the tile, row) block sums of 2^(S*a - m_t)
-    float* bm;             // one pass: per (unit, key tile, row) the reference m_t of those sums
+    float* be;             // one pass: per (unit, key tile, sub-block of the tile, row) sums of 2^(S*a - m_{t,h})
+    float* bm;             // one pass: per (unit, key tile, half-tile, row) the reference m_{t,h} of those sums
     int spt;               // one pass: blocks per key tile (128 / G)
     // element counts of the workspace arrays (checked by the bounds-checked build)
     int64_t lim_items, lim_units, lim_ml, lim_cvec, lim_blk, lim_tok, lim_be, lim_bm;
@@ -103,8 +105,8 @@ struct JobMap {
     int J, W, nbuf, nb_log, wpj;
 };
 __host__ __device__ constexpr int wg_per_job(int J) { return J == 1 ? 4 : J == 2 ? 2 : 1; }
-// PASS 3 is the one-pass form of pass 1 (see epilogue_one_pass): the jobs of pass 1, each TMEM buffer
-// drained whole by one warpgroup.
+// PASS 3 is the one-pass form of pass 1 (epilogue_one_pass_whole / _pairs): the jobs of pass 1, each
+// TMEM buffer drained by one warpgroup, or at d_k = 256 by a pair of warpgroups (64 columns each).
 template <int PASS>
 __host__ __device__ __forceinline__ JobMap job_map(const Params& P) {
     if (PASS == 2 && P.wide2) return JobMap{P.J / 2, 256, 2, 1, 4};
@@ -114,6 +116,16 @@ __host__ __device__ __forceinline__ JobMap job_map(const Params& P) {
 
 // The one pass applies to slabs of 1, 2 or 4 jobs (a warpgroup then always drains the same job).
 __host__ __device__ constexpr bool one_pass_ok(int J) { return J == 1 || J == 2 || J == 4; }
+// Sub-block sums per half-tile (64 keys) of the one pass: the blocks of G <= 64 keys in it, or one.
+__host__ __device__ constexpr int sub_blocks_per_half(int G) { return G >= 64 ? 1 : 64 / G; }
+// The one pass's block sums and their reference maxima per (key tile, row): one maximum and 128 / G
+// sums ("whole" layout) for d_k <= 128, two maxima and the sub-block sums of both halves ("halves"
+// layout) for d_k = 256 (nc = d_k / 64 = 4); see the one-pass section below.
+__host__ __device__ constexpr bool halves_layout(int nc) { return nc == 4; }
+__host__ __device__ constexpr int refs_per_tile(int nc) { return halves_layout(nc) ? 2 : 1; }
+__host__ __device__ constexpr int sums_per_tile(int nc, int G) {
+    return halves_layout(nc) ? 2 * sub_blocks_per_half(G) : kTileKeys / G;
+}
 
 static bool geometry(int Hq, int Hkv, int dk, int n, Geometry* g) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
@@ -158,8 +170,8 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
         // block sums and their reference maxima of the one pass, per (unit, key tile, row); a unit's tiles
         // start at twice its first item's index in the plan's dense per-unit item numbering
         const size_t tiles = static_cast<size_t>(L.items_cap) * kItemTiles;
-        L.be = take(sizeof(float) * tiles * (kTileKeys / G) * g.slab_rows);
-        L.bm = take(sizeof(float) * tiles * g.slab_rows);
+        L.be = take(sizeof(float) * tiles * sums_per_tile(g.nc, G) * g.slab_rows);
+        L.bm = take(sizeof(float) * tiles * refs_per_tile(g.nc) * g.slab_rows);
     }
     L.total = o;
     return L;
@@ -303,6 +315,7 @@ struct Smem {
     uint64_t* slab_full;
     uint64_t* slab_free;
     uint64_t* mma_done;    // [kIssuers]
+    uint64_t* tok;         // [2]        turn of issuer 0 / 1 to issue its next job (jobs-outer path)
     uint32_t* tmem_holder;
     int* abort_flag;
     float* cvec;           // [kCvecFloats]
@@ -323,7 +336,8 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
     s.slab_full = b + 2 * kStages + 8;
     s.slab_free = b + 2 * kStages + 9;
     s.mma_done = b + 2 * kStages + 10;
-    s.tmem_holder = reinterpret_cast<uint32_t*>(b + 2 * kStages + 10 + kIssuers);
+    s.tok = b + 2 * kStages + 10 + kIssuers;
+    s.tmem_holder = reinterpret_cast<uint32_t*>(b + 2 * kStages + 12 + kIssuers);
     s.abort_flag = reinterpret_cast<int*>(s.tmem_holder + 1);
     s.cvec = reinterpret_cast<float*>(ctrl + kCtrlBytes);
     s.xchg = reinterpret_cast<uint8_t*>(s.cvec + kCvecFloats);
@@ -440,14 +454,21 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
 // the advance is a plain add on the descriptor.
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Three issuer warps share the jobs by TMEM buffer: issuer w issues the jobs whose buffer b has
-// b mod 3 == w.  A tcgen05.commit holds up the thread that issues it until its earlier MMAs have
-// drained, so an issuer keeps one job in flight, and around each job it spends a few hundred cycles
-// in the commit, the buffer wait and its loop (cycle-stamped timelines); several issuers keep several
-// jobs in flight.  A commit tracks only its own thread's MMAs, so every barrier
-// that releases an operand (K stage, query slab) takes one commit from each issuer, and each
-// issuer waits for a stage to land before it commits the stage's release, even when it issued no
-// job on that tile: its arrival can then never count toward a later use of the stage.
+// Three issuer warps.  A tcgen05.mma returns to its thread only once the tensor core's queue has room
+// (about five 128 x 128 x 16 steps, ~320 cycles of work), so an issuer runs at most that far ahead of
+// the pipe; a commit returns after ~55 cycles but holds the thread's next MMAs until the ones it tracks
+// have completed (timed on this part: ~80 idle cycles per commit when no other thread's MMAs are
+// queued).  Several issuers keep the queue filled across each other's commits and waits.
+//   jobs outer (d_k <= 128)  issuers 0 and 1 take the even and odd jobs of the running job count (TMEM
+//       buffers 0, 2 and 1, 3) and hand the turn to issue to each other through an mbarrier after
+//       each job, so the tensor core receives whole jobs in order and they complete one after
+//       another, while each issuer's commit, buffer wait and loop overlap the other's MMAs.
+//   chunks outer (d_k = 256)  issuer w issues the jobs whose buffer b has b mod 3 == w.
+// Every use of a TMEM buffer comes from the same warp in order, so its waits for the buffer always
+// refer to the phase just before the current one.  A commit tracks only its own thread's MMAs, so
+// every barrier that releases an operand (K stage, query slab) takes one commit from each issuer,
+// and each issuer waits for a stage to land before it commits the stage's release, even when it
+// issued no job on that tile: its arrival can then never count toward a later use of the stage.
 static_assert(kThreads == 640 && kIssuer1Warp + kIssuers - 2 == kThreads / 32 - 1,
               "warps: producer 0, issuers 1, 18 and 19, epilogue 2-17");
 template <int PASS, int NC>
@@ -472,10 +493,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
         if (leader) tc_commit(bar);
         __syncwarp();
     };
-    // every use of a TMEM buffer is issued by the same warp (buffer b by issuer b mod kIssuers): its waits
-    // for the buffer then always refer to the phase just before the current one, whatever the other
-    // issuers do (with jobs handed out round-robin an issuer could run two uses ahead on a buffer and
-    // read its parity from the wrong phase)
+    // chunks outer: buffer b by issuer b mod kIssuers (with jobs handed out round-robin an issuer could
+    // run two uses ahead on a buffer and read its parity from the wrong phase)
     auto mine = [&](uint32_t q) { return (q & (jm.nbuf - 1)) % kIssuers == w; };
     int4 na, nb;
     item_load(P, it0, it1, na, nb);
@@ -495,8 +514,11 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                 bool landed = false;
                 for (int j = 0; j < J; ++j) {
                     const uint32_t q = jc + j, buf = q & (jm.nbuf - 1);
-                    if (!mine(q)) continue;
+                    if ((q & 1u) != w) continue;
                     if (!wait_all(smem_u32(S.tempty + buf), ((q >> jm.nb_log) & 1) ^ 1)) goto out;
+                    // this issuer's turn: the other one has issued job q - 1 (issuer 0's first job has no wait)
+                    const int turn = static_cast<int>(q >> 1) - (w == 0 ? 1 : 0);
+                    if (turn >= 0 && !wait_all(smem_u32(S.tok + w), turn & 1)) goto out;
                     tc_fence_after();
                     const uint64_t qd = desc_add(slab_d0, j * jm.W * 128);
                     const uint32_t d_tmem = tmem_base + buf * jm.W;
@@ -517,6 +539,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                         }
                     }
                     landed = true;
+                    if (leader) mbar_arrive(smem_u32(S.tok + (w ^ 1u)));       // job q + 1's turn
+                    __syncwarp();
                     commit(smem_u32(S.tfull + buf));
                 }
 #pragma unroll
@@ -988,9 +1012,14 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
 // Per window row j and key tile t, the thread that owns row j (rows are TMEM lanes) computes with its
 // running maximum m_t (base 2, over the keys it has seen up to the end of tile t) the sums
 //   e_{j,g} = sum_{i in B_g} 2^(S_ji * a - m_t)      for the 128 / G blocks g of tile t,
-// and writes them with m_t.  The usual (m, l) partials per work item are written as in pass 1, so the
-// merge kernel gives c_j = m_j + log2(l_j), and the reduce kernel then forms Eq. 4 exactly:
-//   sum_j sum_{i in B_g} A_ji = sum_j e_{j,g} * 2^(m_t - c_j).
+// and writes them with m_t ("whole" layout, d_k <= 128).  At d_k = 256 each tile is read in two halves
+// of 64 keys by two threads that own row j ("halves" layout): the thread of half h keeps its own
+// running maximum m_{t,h} and writes the sums over the sub-blocks s of its half (the blocks of G <= 64
+// keys in it, or its 64 keys of a 128-key block) with m_{t,h}.  The (m, l) partials per work item
+// (merged over the threads that hold a row) are written as in pass 1, so the merge kernel gives
+// c_j = m_j + log2(l_j), and the reduce kernel then forms Eq. 4 exactly:
+//   sum_j sum_{i in B_g} A_ji = sum_j e_{j,g} * 2^(m_t - c_j)                   (whole)
+//                             = sum_j sum_{s in B_g} e_{j,s} * 2^(m_{t,h(s)} - c_j)   (halves).
 // This is the two-pass softmax of the section 3.5 kernel design with the second pass run over the block
 // sums (G times smaller than S) instead of over a recomputed S: the tensor work and the exponentials of
 // the recompute pass disappear; S itself is never stored.
@@ -1003,15 +1032,15 @@ __device__ __forceinline__ void mask_chunk(uint32_t (&v)[16], int ch, int lim) {
         if (16 * ch + c > lim) v[c] = 0xFF800000u;
 }
 
-// 32 columns (the 16-column chunks 2*h2 and 2*h2+1) of this thread's row in the one pass: fold their
-// maximum into m (rescaling the block sums of the tile so far and the l of the item's earlier tiles when
-// it grows), then add 2^(S*a - m) over each chunk to its block's sum e[chunk / CPB] (CPB = G / 16 chunks
-// per block).  One maximum update per 32 columns leaves 32 independent exponentials behind it (measured
-// 2-8% faster score calls than an update per 16 columns).  Columns outside the causal range arrive as
-// -inf and add 0.
-template <int CPB>
+// 32 columns (the 16-column chunks 2*h2 and 2*h2+1 of this thread's half-tile) of its row in the one
+// pass: fold their maximum into m (rescaling the sub-block sums of the half-tile so far and the l of the
+// item's earlier tiles when it grows), then add 2^(S*a - m) over each chunk to its sub-block's sum
+// e[chunk / CPB] (CPB = G / 16 chunks per block; a 128-key block has one sub-block per half).  One
+// maximum update per 32 columns leaves 32 independent exponentials behind it (measured 2-8% faster
+// score calls than an update per 16 columns).  Columns outside the causal range arrive as -inf and add 0.
+template <int CPB, int NE>
 __device__ __forceinline__ void one_pass_chunk32(const uint32_t (&v)[32], int h2, float a, float& m, float& l,
-                                                 float (&e)[8 / CPB]) {
+                                                 float (&e)[NE]) {
     float x[6];
 #pragma unroll
     for (int i = 0; i < 5; ++i) x[i] = max3(f(v[6 * i]), f(v[6 * i + 1]), f(v[6 * i + 2]));
@@ -1024,7 +1053,7 @@ __device__ __forceinline__ void one_pass_chunk32(const uint32_t (&v)[32], int h2
         const float sc = ex2(m - mx);           // 0 while m = -inf
         l *= sc;
 #pragma unroll
-        for (int b = 0; b < 8 / CPB; ++b)
+        for (int b = 0; b < NE; ++b)
             if (b <= (2 * h2 + 1) / CPB) e[b] *= sc;
         m = mx;
     }
@@ -1045,6 +1074,31 @@ __device__ __forceinline__ void one_pass_chunk32(const uint32_t (&v)[32], int h2
     }
 }
 
+// one half-tile (64 columns) of one job for this thread's row, the TMEM buffer released as soon as its
+// last columns have landed; `masked` (warp-uniform) applies the causal limit lim (relative to the
+// half's first column)
+template <int CPB, int NE>
+__device__ __forceinline__ void one_pass_half(const Smem& S, uint32_t ta, uint32_t buf, int lane, bool masked, int lim,
+                                              float a, float& m, float& l, float (&e)[NE]) {
+    // two 32-column loads, the second in flight while the first is reduced
+    uint32_t va[32], vb[32];
+    tmem_ld32(ta, va);
+    tmem_wait_pin32(va);
+    tmem_ld32(ta + 32, vb);
+    if (masked) {
+        mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[0]), 0, lim);
+        mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[16]), 1, lim);
+    }
+    one_pass_chunk32<CPB, NE>(va, 0, a, m, l, e);
+    tmem_wait_pin32(vb);
+    release_tmem(S, buf, lane);
+    if (masked) {
+        mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[0]), 2, lim);
+        mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[16]), 3, lim);
+    }
+    one_pass_chunk32<CPB, NE>(vb, 1, a, m, l, e);
+}
+
 // one whole 128-column job of this thread's row, the buffer released as soon as its last columns have
 // landed; `masked` (warp-uniform) applies the causal limit lim
 template <int CPB>
@@ -1062,7 +1116,7 @@ __device__ __forceinline__ void one_pass_tile(const Smem& S, uint32_t ta, uint32
             mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[0]), 2 * h, lim);
             mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&va[16]), 2 * h + 1, lim);
         }
-        one_pass_chunk32<CPB>(va, h, a, m, l, e);
+        one_pass_chunk32<CPB, 8 / CPB>(va, h, a, m, l, e);
         tmem_wait_pin32(vb);
         if (h + 2 < 4) tmem_ld32(ta + (h + 2) * 32, va);
         else release_tmem(S, buf, lane);
@@ -1070,16 +1124,18 @@ __device__ __forceinline__ void one_pass_tile(const Smem& S, uint32_t ta, uint32
             mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[0]), 2 * h + 2, lim);
             mask_chunk(*reinterpret_cast<uint32_t(*)[16]>(&vb[16]), 2 * h + 3, lim);
         }
-        one_pass_chunk32<CPB>(vb, h + 1, a, m, l, e);
+        one_pass_chunk32<CPB, 8 / CPB>(vb, h + 1, a, m, l, e);
         if (h + 2 < 4) tmem_wait_pin32(va);
     }
 }
 
-// Warpgroup w drains TMEM buffer w: with J in {1, 2, 4} jobs per tile that is always job w % J (the
-// same 128 window rows), on every (4 / J)-th tile of the CTA's sequence.  The warpgroups that hold the
+// d_k <= 128 (the jobs-outer issue order): warpgroup w drains TMEM buffer w whole; with J in {1, 2, 4}
+// jobs per tile that is always job w % J (the same 128 window rows), on every (4 / J)-th tile of the
+// CTA's sequence.  (The pairs of epilogue_one_pass_pairs measured 17-30% slower here: a thread then
+// pays the first TMEM load and the per-job bookkeeping twice per tile.)  The warpgroups that hold the
 // same rows merge their (m, l) at the end of each item in a fixed order, as in pass 1.  CPB = G / 16.
 template <int CPB>
-__device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
+__device__ void epilogue_one_pass_whole(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
     constexpr int SPT = 8 / CPB;                // blocks per tile
     volatile int* abort_flag = S.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1161,6 +1217,114 @@ __device__ void epilogue_one_pass(const Params& P, const Smem& S, uint32_t tmem_
     }
 }
 
+// d_k = 256 (the chunks-outer issue order): the four epilogue warpgroups form two pairs; pair p drains
+// the jobs q (running job count) with
+// q mod 2 = p, which are those in TMEM buffers p and p + 2, and in each job warpgroup 2p + h reads
+// the columns 64h .. 64h + 63.  With J = 4 jobs per tile a pair holds the rows of jobs p and p + 2 (two
+// rows per thread), with J = 2 those of job p, and with J = 1 the pairs take alternate tiles of the
+// one job.  A job is drained by eight warps, so its TMEM buffer comes free in about half the time one
+// warpgroup takes, and consecutive jobs (issued in order, see mma_issuer) drain on different pairs:
+// the exponentials of one job overlap the MMAs of the next.  The threads that hold a row merge their
+// (m, l) at the end of each item in a fixed order, as in pass 1.  CPB = G / 16.
+template <int CPB>
+__device__ void epilogue_one_pass_pairs(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
+    constexpr int NE = sub_blocks_per_half(16 * CPB);   // sub-block sums per half-tile
+    constexpr int SB = 2 * NE;                          // per tile
+    volatile int* abort_flag = S.abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = (warp - 2) >> 2;             // warpgroup 0..3
+    const int pair = wg >> 1, h = wg & 1;       // jobs q with q % 2 == pair; columns 64h ..
+    const int qd = warp & 3;                    // TMEM lane quarter this warp may access
+    const int rl = qd * 32 + lane;
+    const int J = P.J;
+    const int nrow = J >= 2 ? J / 2 : 1;        // rows (jobs) per thread
+    const float a = P.a;
+    const uint32_t ta0 = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + 64 * h;
+    auto job_of = [&](int u) { return J >= 2 ? pair + 2 * u : 0; };
+    uint32_t tiles_done = 0;
+    int prev_slab = -1;
+    bool rin[2] = {false, false};
+    int rmod[2] = {0, 0};
+    for (int it = it0; it < it1; ++it) {
+        int4 ia, ib;
+        item_load(P, it, it1, ia, ib);
+        const ItemInfo I = item_decode(P, ia, ib);
+        if (I.slab != prev_slab) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (u >= nrow) break;
+                const int qg = I.slab * P.slab_rows + job_of(u) * 128 + rl;
+                rin[u] = qg < P.rows_total;
+                rmod[u] = qg % P.n;
+            }
+            prev_slab = I.slab;
+        }
+        const int2 ui = P.unit_items[I.unit];
+        const size_t tile0 = static_cast<size_t>(ui.x) * kItemTiles;   // the unit's first key tile
+        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                if (u >= nrow) break;
+                const uint32_t q = tiles_done * J + job_of(u);
+                if ((q & 1u) != static_cast<uint32_t>(pair)) continue;          // the other pair's tile (J = 1)
+                const uint32_t buf = q & 3u;
+                const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (q >> 2) & 1, abort_flag));
+                tc_fence_after();
+                if (!ok) {
+                    release_tmem(S, buf, lane);
+                    continue;
+                }
+                const int row = job_of(u) * 128 + rl;
+                const int pos = I.N - P.n + rmod[u];                         // this row's position in the request
+                const int lim = rin[u] && pos >= 0 ? pos - kt * kTileKeys - 64 * h : -1;   // last visible column
+                float e[NE];
+#pragma unroll
+                for (int b = 0; b < NE; ++b) e[b] = 0.f;
+                const bool masked = !__all_sync(0xffffffffu, lim >= 63);
+                one_pass_half<CPB, NE>(S, ta0 + buf * 128, buf, lane, masked, lim, a, m[u], l[u], e);
+                const size_t t = tile0 + kt;
+                const size_t mi = (t * 2 + h) * P.slab_rows + row;
+                if (UP_IN(mi, P.lim_bm, P.status)) P.bm[mi] = m[u];
+                float ts = 0.f;
+#pragma unroll
+                for (int b = 0; b < NE; ++b) {
+                    const size_t ei = (t * SB + h * NE + b) * P.slab_rows + row;
+                    if (UP_IN(ei, P.lim_be, P.status)) P.be[ei] = e[b];
+                    ts += e[b];
+                }
+                l[u] += ts;
+            }
+        }
+        // this item's (m, l) partial of each row, merged over the threads that hold the row: the two
+        // halves of its pair (a barrier of the pair only, so that the pairs stay independent), and with
+        // J = 1 both pairs
+        float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;
+        float2* xm = reinterpret_cast<float2*>(S.xchg);                      // [4 warpgroups][2 rows][128]
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (u < nrow) xm[(wg * 2 + u) * 128 + rl] = make_float2(m[u], l[u]);
+        const int bar_id = J >= 2 ? 1 + pair : 3, bar_n = J >= 2 ? kEpiThreads / 2 : kEpiThreads;
+        named_bar_sync(bar_id, bar_n);
+        const int wfirst = J >= 2 ? 2 * pair : 0, wcount = J >= 2 ? 2 : 4;
+        if (wg == wfirst) {
+            for (int u = 0; u < nrow; ++u) {        // (m, l) from shared memory: no register arrays indexed here
+                float mm = -INFINITY;
+                for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) mm = fmaxf(mm, xm[(w2 * 2 + u) * 128 + rl].x);
+                float ll = 0.f;
+                if (mm > -INFINITY)
+                    for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) {
+                        const float2 x = xm[(w2 * 2 + u) * 128 + rl];
+                        ll += x.y * ex2(x.x - mm);
+                    }
+                const int row = job_of(u) * 128 + rl;
+                if (UP_IN(part + (size_t)row * ui.y - P.ml, P.lim_ml, P.status)) part[(size_t)row * ui.y] = make_float2(mm, ll);
+            }
+        }
+        named_bar_sync(bar_id, bar_n);
+    }
+}
+
 // Fold each query row's pass-1 partials (one per work item of its unit, in the unit's key-tile order)
 // into c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
 __global__ void __launch_bounds__(256) merge_kernel(Params P) {
@@ -1221,11 +1385,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = 0; b < 4; ++b) {
             mbar_init(smem_u32(S.tfull + b), 1);
             // one arrival per epilogue warp that reads the job: 4 warps per warpgroup on it
-            mbar_init(smem_u32(S.tempty + b), 4 * job_map<PASS>(P).wpj);
+            mbar_init(smem_u32(S.tempty + b), 4 * (PASS == 3 && NC == 4 ? 2 : job_map<PASS>(P).wpj));
         }
         mbar_init(smem_u32(S.slab_full), 1);
         mbar_init(smem_u32(S.slab_free), kIssuers);
         for (int w = 0; w < kIssuers; ++w) mbar_init(smem_u32(S.mma_done + w), 1);
+        for (int w = 0; w < 2; ++w) mbar_init(smem_u32(S.tok + w), 1);
         *S.abort_flag = 0;
         fence_mbar_init();
     }
@@ -1266,12 +1431,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp >= kIssuer1Warp) {
         // warps 1, 18 and 19 (kThreads covers exactly these and the producer and epilogue warps)
         mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : static_cast<uint32_t>(warp - kIssuer1Warp + 1));
-    } else if (PASS == 3) {
+    } else if (PASS == 3 && NC == 4) {
         switch (P.spt) {                         // blocks per key tile = 128 / G
-            case 8: epilogue_one_pass<1>(P, S, tmem_base, it0, it1); break;
-            case 4: epilogue_one_pass<2>(P, S, tmem_base, it0, it1); break;
-            case 2: epilogue_one_pass<4>(P, S, tmem_base, it0, it1); break;
-            default: epilogue_one_pass<8>(P, S, tmem_base, it0, it1); break;
+            case 8: epilogue_one_pass_pairs<1>(P, S, tmem_base, it0, it1); break;
+            case 4: epilogue_one_pass_pairs<2>(P, S, tmem_base, it0, it1); break;
+            case 2: epilogue_one_pass_pairs<4>(P, S, tmem_base, it0, it1); break;
+            default: epilogue_one_pass_pairs<8>(P, S, tmem_base, it0, it1); break;
+        }
+    } else if (PASS == 3) {
+        switch (P.spt) {
+            case 8: epilogue_one_pass_whole<1>(P, S, tmem_base, it0, it1); break;
+            case 4: epilogue_one_pass_whole<2>(P, S, tmem_base, it0, it1); break;
+            case 2: epilogue_one_pass_whole<4>(P, S, tmem_base, it0, it1); break;
+            default: epilogue_one_pass_whole<8>(P, S, tmem_base, it0, it1); break;
         }
     } else {
         const JobMap jm = job_map<PASS>(P);
@@ -1352,12 +1524,15 @@ constexpr int kMaxUnitsPerReq = 1024;
 
 __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
 
-template <int SPT>
+template <int SPT, bool HALVES>
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
     pdl_wait();
     pdl_trigger();
     if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
-    constexpr int B = SPT <= 2 ? 4 : SPT == 4 ? 2 : 1;       // (unit, row group) pairs per thread in flight
+    // sums per half-tile and per tile, reference maxima per tile (see halves_layout)
+    constexpr int NE = HALVES ? sub_blocks_per_half(kTileKeys / SPT) : SPT, SB = HALVES ? 2 * NE : SPT;
+    constexpr int NR = HALVES ? 2 : 1;
+    constexpr int B = SB <= 2 ? 4 : SB == 4 ? 2 : 1;         // (unit, row group) pairs per thread in flight
     __shared__ float s_part[kReduceThreads / 32][SPT];
     __shared__ int s_tile0[kMaxUnitsPerReq];
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -1393,37 +1568,44 @@ __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
 #pragma unroll
         for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
         for (int i0 = threadIdx.x; i0 < pairs; i0 += B * kReduceThreads) {
-            float4 wv[B], ev[B][SPT];
+            float4 wv[B][NR], ev[B][SB];
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 const int i = i0 + b * kReduceThreads;
-                if (i < pairs) {
-                    const int kk = i / rows4, r0 = (i - kk * rows4) * 4;
-                    const size_t t = static_cast<size_t>(s_tile0[kk]) + tile;
-                    if (!UP_IN(t * rows + r0 + 3, P.lim_bm, P.status) ||
-                        !UP_IN((t * SPT + SPT - 1) * rows + r0 + 3, P.lim_be, P.status) ||
-                        !UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status)) {
-                        wv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                        for (int s = 0; s < SPT; ++s) ev[b][s] = make_float4(0.f, 0.f, 0.f, 0.f);
-                        continue;
-                    }
-                    const float4 m4 = ldcg4(P.bm + t * rows + r0);
-                    const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
-#pragma unroll
-                    for (int s = 0; s < SPT; ++s) ev[b][s] = ldcg4(P.be + (t * SPT + s) * rows + r0);
-                    wv[b] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
-                } else {
-                    wv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int s = 0; s < SPT; ++s) ev[b][s] = make_float4(0.f, 0.f, 0.f, 0.f);
+                bool live = i < pairs;
+                size_t t = 0;
+                int kk = 0, r0 = 0;
+                if (live) {
+                    kk = i / rows4;
+                    r0 = (i - kk * rows4) * 4;
+                    t = static_cast<size_t>(s_tile0[kk]) + tile;
+                    live = UP_IN((t * NR + NR - 1) * rows + r0 + 3, P.lim_bm, P.status) &&
+                           UP_IN((t * SB + SB - 1) * rows + r0 + 3, P.lim_be, P.status) &&
+                           UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status);
                 }
+                if (!live) {
+#pragma unroll
+                    for (int hh = 0; hh < NR; ++hh) wv[b][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int sb = 0; sb < SB; ++sb) ev[b][sb] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    continue;
+                }
+                const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
+#pragma unroll
+                for (int hh = 0; hh < NR; ++hh) {
+                    const float4 m4 = ldcg4(P.bm + (t * NR + hh) * rows + r0);
+                    wv[b][hh] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
+                }
+#pragma unroll
+                for (int sb = 0; sb < SB; ++sb) ev[b][sb] = ldcg4(P.be + (t * SB + sb) * rows + r0);
             }
 #pragma unroll
             for (int b = 0; b < B; ++b)
 #pragma unroll
-                for (int s = 0; s < SPT; ++s)
-                    acc[s] += (ev[b][s].x * wv[b].x + ev[b][s].y * wv[b].y) + (ev[b][s].z * wv[b].z + ev[b][s].w * wv[b].w);
+                for (int sb = 0; sb < SB; ++sb) {
+                    const float4 w4 = wv[b][sb / NE], e4 = ev[b][sb];
+                    acc[SB == SPT ? sb : 0] += (e4.x * w4.x + e4.y * w4.y) + (e4.z * w4.z + e4.w * w4.w);
+                }
         }
 #pragma unroll
         for (int s = 0; s < SPT; ++s) {
@@ -1523,11 +1705,12 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
     e = launch_merge(P, merge_rows, st);
     if (e != cudaSuccess) return e;
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(req_tiles, 8 * num_sms())));
+    constexpr bool H = halves_layout(NC);
     switch (P.spt) {
-        case 8: e = launch_pdl(reduce_kernel<8>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        case 4: e = launch_pdl(reduce_kernel<4>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        case 2: e = launch_pdl(reduce_kernel<2>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        default: e = launch_pdl(reduce_kernel<1>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 8: e = launch_pdl(reduce_kernel<8, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 4: e = launch_pdl(reduce_kernel<4, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 2: e = launch_pdl(reduce_kernel<2, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        default: e = launch_pdl(reduce_kernel<1, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
     }
     count_launch();
     return e;
@@ -1608,8 +1791,8 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.lim_cvec = L.units * g.slab_rows;
     P.lim_blk = static_cast<int64_t>(Hkv) * g.slabs * 4 * nb_cap;
     P.lim_tok = token_scores ? static_cast<int64_t>(Hkv) * g.slabs * 4 * T : 0;
-    P.lim_be = one_pass ? L.items_cap * kItemTiles * (kTileKeys / G) * g.slab_rows : 0;
-    P.lim_bm = one_pass ? L.items_cap * kItemTiles * g.slab_rows : 0;
+    P.lim_be = one_pass ? L.items_cap * kItemTiles * sums_per_tile(g.nc, G) * g.slab_rows : 0;
+    P.lim_bm = one_pass ? L.items_cap * kItemTiles * refs_per_tile(g.nc) * g.slab_rows : 0;
     P.block_scores = block_scores;
     P.token_scores = token_scores;
     P.status = dev_status;
