@@ -180,8 +180,9 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
 // ------------------------------------------------------------------------------------------------
 // plan: validate the varlen metadata and lay out the work items (one CTA)
 
-__device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sh, int* total) {
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+// exclusive prefix sum over the CTA (blockDim.x a multiple of 32, at most 1024); sh holds 32 ints
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sh, int* total) {
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5, nw = blockDim.x >> 5;
     int x = v;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -191,13 +192,13 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sh, int* to
     if (lane == 31) sh[w] = x;
     __syncthreads();
     if (w == 0) {
-        int s = sh[lane];
+        int s = lane < nw ? sh[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             int y = __shfl_up_sync(0xffffffffu, s, o);
             if (lane >= o) s += y;
         }
-        sh[lane] = s;   // inclusive over warps
+        sh[lane] = s;   // inclusive over warps (warps past the last add 0)
     }
     __syncthreads();
     const int before = (w > 0 ? sh[w - 1] : 0) + x - v;
@@ -211,6 +212,7 @@ __device__ __forceinline__ int block_exclusive_scan_1024(int v, int* sh, int* to
 // unit offsets in global memory).
 constexpr int kPlanThreads = 1024;
 constexpr int kPlanSmemReqs = 4096;
+constexpr int kPlanScratch = (kPlanSmemReqs + 64) * 4;   // bytes of the query slab a planning pass borrows
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
     pdl_wait();
@@ -249,7 +251,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
     int local = 0;
     for (int r = r0; r < r1; ++r) local += nitems(r) * P.units_per_req;
     int total = 0;
-    int off = block_exclusive_scan_1024(local, s_scan, &total);
+    int off = block_exclusive_scan(local, s_scan, &total);
     for (int r = r0; r < r1; ++r) {
         const int ni = nitems(r);
         if (blockIdx.x == 0) {
@@ -293,13 +295,93 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(Params P) {
         const int ntiles = (N + kTileKeys - 1) / kTileKeys;
         if (UP_IN(it, P.lim_items, P.status)) {
             P.items[2 * it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
-            P.items[2 * it + 1] = make_int4(P.cu[r], N, 0, 0);
+            P.items[2 * it + 1] = make_int4(P.cu[r], N, first(r) * NS + kk * ni, ni);
         }
     }
     if (tid == 0 && blockIdx.x == 0) {
         P.n_items[0] = total;
         P.n_items[1] = 1;          // metadata validated
     }
+}
+
+// Up to kPlanSmemReqs requests the one pass plans inside its own launch (no plan kernel before it):
+// every CTA validates the metadata, scans the requests' item counts into shared memory and writes the
+// entries of its own items [it0, it1) and the unit offsets of the requests r with
+// r mod gridDim.x == blockIdx.x (read by the merge and reduce kernels); CTA 0 writes the item count.
+// The list and the split over the CTAs are those of plan_kernel.  False when the metadata is invalid
+// (CTA 0 records the status; every CTA returns false and does no work).  All threads call it; s_first
+// holds kPlanSmemReqs ints and s_red 33.
+__device__ bool plan_prologue(const Params& P, int* s_first, int* s_red, int& it0, int& it1) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    if (tid == 0) s_red[32] = 0;
+    __syncthreads();
+    for (int r = tid; r < P.R; r += nt) {
+        const int c0 = P.cu[r], c1 = P.cu[r + 1];
+        if ((r == 0 && c0 != 0) || c1 < c0 || c1 > P.T || (r == P.R - 1 && c1 != P.T)) atomicOr(&s_red[32], 1);
+        const int nb = (c1 - c0 + P.G - 1) / P.G;
+        const int b0 = P.cb[r], b1 = P.cb[r + 1];
+        if ((r == 0 && b0 != 0) || b1 - b0 != nb || (int64_t)b1 > P.nb_cap) atomicOr(&s_red[32], 2);
+    }
+    __syncthreads();
+    const int bad = s_red[32];
+    if (bad) {
+        if (tid == 0 && blockIdx.x == 0) {
+            set_status(P.status, (bad & 1) ? UP_DEV_BAD_CU_SEQLENS : UP_DEV_BAD_CU_BLOCKS);
+            P.n_items[0] = 0;
+            P.n_items[1] = 0;
+        }
+        it0 = it1 = 0;
+        return false;
+    }
+    const int NS = P.nsets, upr = P.units_per_req;
+    auto nitems = [&](int r) {
+        const int N = P.cu[r + 1] - P.cu[r];
+        return ((N + kTileKeys - 1) / kTileKeys + kItemTiles - 1) / kItemTiles;
+    };
+    const int per = (P.R + nt - 1) / nt;
+    const int r0 = min(P.R, tid * per), r1 = min(P.R, r0 + per);
+    int local = 0;
+    for (int r = r0; r < r1; ++r) local += nitems(r) * upr;
+    int total = 0;
+    int off = block_exclusive_scan(local, s_red, &total);
+    for (int r = r0; r < r1; ++r) {
+        const int ni = nitems(r);
+        if (r % gridDim.x == blockIdx.x)
+            for (int kk = 0; kk < upr; ++kk) {
+                const int u = r * upr + kk;
+                if (UP_IN(u, P.lim_units, P.status)) P.unit_items[u] = make_int2(off + kk * ni, ni);
+            }
+        s_first[r] = off / NS;
+        off += ni * upr;
+    }
+    if (tid == 0 && blockIdx.x == 0) {
+        P.n_items[0] = total;
+        P.n_items[1] = 1;
+    }
+    __syncthreads();
+    const int groups = gridDim.x / NS, run = total / NS;
+    const int set = blockIdx.x / groups, g = blockIdx.x % groups;
+    it0 = set * run + static_cast<int>((int64_t)g * run / groups);
+    it1 = set * run + static_cast<int>((int64_t)(g + 1) * run / groups);
+    for (int it = it0 + tid; it < it1; it += nt) {
+        const int rel = it - set * run;
+        int lo = 0, hi = P.R;
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (s_first[mid] <= rel) lo = mid; else hi = mid;
+        }
+        const int r = lo, ni = nitems(r);
+        const int rel2 = rel - s_first[r];
+        const int kq = rel2 / ni, sidx = rel2 % ni;
+        const int kk = kq * NS + set;
+        const int N = P.cu[r + 1] - P.cu[r];
+        const int ntiles = (N + kTileKeys - 1) / kTileKeys;
+        if (UP_IN(it, P.lim_items, P.status)) {
+            P.items[2 * it] = make_int4(r, kk, sidx * kItemTiles, min(ntiles, (sidx + 1) * kItemTiles));
+            P.items[2 * it + 1] = make_int4(P.cu[r], N, s_first[r] * NS + kk * ni, ni);
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -346,6 +428,7 @@ __device__ __forceinline__ Smem carve(uint8_t* raw) {
 
 struct ItemInfo {
     int r, kk, tb, te, unit, base, N, kh, slab;
+    int2 ui;               // the unit's first item in the per-unit numbering, and its item count
 };
 
 // Values read from memory are not known to be warp-uniform; the MMA, TMA and TMEM-load operands
@@ -354,7 +437,8 @@ struct ItemInfo {
 __device__ __forceinline__ int uni(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 // An item is two entries of the list: (request, unit of the request, first tile, end tile) and (the
-// request's first token, its length), loaded together (no dependent loads).  The producer and the MMA
+// request's first token, its length, the unit's first item in the per-unit numbering, the unit's item
+// count), loaded together (no dependent loads).  The producer and the MMA
 // issuers, which set the pace, load the next item's entries while they work on the current one.
 __device__ __forceinline__ void item_load(const Params& P, int it, int it1, int4& a, int4& b) {
     if (it < it1 && UP_IN(it, P.lim_items, P.status)) {
@@ -373,6 +457,7 @@ __device__ __forceinline__ ItemInfo item_decode(const Params& P, const int4& a, 
     I.unit = I.r * P.units_per_req + I.kk;
     I.base = uni(b.x);
     I.N = uni(b.y);
+    I.ui = make_int2(uni(b.z), uni(b.w));
     I.kh = I.kk / P.slabs;
     I.slab = I.kk % P.slabs;
     return I;
@@ -972,7 +1057,7 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
         if (PASS == 1) {
             // merge the warpgroups that share a job (fixed order), write this item's partial (m, l)
             // into the unit's block, laid out [row][item of the unit] for the merge kernel
-            const int2 ui = P.unit_items[I.unit];
+            const int2 ui = I.ui;
             float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;   // tile pair in the unit
             float2* xm = reinterpret_cast<float2*>(S.xchg);             // [4 warpgroups][2 jobs][128 rows]
             if (wpj > 1) {
@@ -1163,7 +1248,7 @@ __device__ void epilogue_one_pass_whole(const Params& P, const Smem& S, uint32_t
         }
         const int pos = I.N - P.n + rmod;       // this row's position in the request
         const bool rvalid = rin && pos >= 0;
-        const int2 ui = P.unit_items[I.unit];
+        const int2 ui = I.ui;
         const size_t tile0 = static_cast<size_t>(ui.x) * kItemTiles;   // the unit's first key tile
         float m = -INFINITY, l = 0.f;
         for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
@@ -1259,7 +1344,7 @@ __device__ void epilogue_one_pass_pairs(const Params& P, const Smem& S, uint32_t
             }
             prev_slab = I.slab;
         }
-        const int2 ui = P.unit_items[I.unit];
+        const int2 ui = I.ui;
         const size_t tile0 = static_cast<size_t>(ui.x) * kItemTiles;   // the unit's first key tile
         float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
         for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
@@ -1327,16 +1412,13 @@ __device__ void epilogue_one_pass_pairs(const Params& P, const Smem& S, uint32_t
 
 // Fold each query row's pass-1 partials (one per work item of its unit, in the unit's key-tile order)
 // into c = m + log2(l): one warp per (unit, row), lanes over the items, fixed shuffle trees.
-__global__ void __launch_bounds__(256) merge_kernel(Params P) {
-    pdl_wait();
-    pdl_trigger();
-    if (__ldcg(P.n_items + 1) == 0) return;
+// warp gw of nw (whole warps) folds the rows gw, gw + nw, ...
+__device__ void merge_rows(const Params& P, int64_t gw, int64_t nw) {
     const int lane = threadIdx.x & 31;
     const int64_t rows_all = (int64_t)P.R * P.units_per_req * P.slab_rows;
-    const int64_t wstride = (int64_t)gridDim.x * (blockDim.x >> 5);
-    for (int64_t gr = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); gr < rows_all; gr += wstride) {
+    for (int64_t gr = gw; gr < rows_all; gr += nw) {
         const int u = static_cast<int>(gr / P.slab_rows), row = static_cast<int>(gr % P.slab_rows);
-        const int2 ui = P.unit_items[u];
+        const int2 ui = __ldcg(&P.unit_items[u]);
         const float2* part = P.ml + (size_t)ui.x * P.slab_rows + (size_t)row * ui.y;
         if (!UP_IN(u, P.lim_units, P.status) || !UP_IN(part + ui.y - 1 - P.ml, P.lim_ml, P.status)) continue;
         // the first kCache partials of each lane stay in registers between the max and the sum (one
@@ -1370,7 +1452,139 @@ __global__ void __launch_bounds__(256) merge_kernel(Params P) {
     }
 }
 
-template <int PASS, int NC>
+__global__ void __launch_bounds__(256) merge_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
+    if (__ldcg(P.n_items + 1) == 0) return;
+    merge_rows(P, (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), (int64_t)gridDim.x * (blockDim.x >> 5));
+}
+
+// The one pass's Eq. 4: a CTA forms the SPT = 128 / G block scores of one (request, key tile) at a time
+//   b_g = 1/(n_eff * Hq * G) * sum over the request's units and their rows j of e_{j,g} * 2^(m_t,j - c_j)
+// (each CTA takes a contiguous range of these tasks).  Threads take (unit, group of 4 rows) pairs in a
+// fixed assignment, with 16-byte loads, several pairs' loads in flight before any is used; per-thread
+// sums are reduced by warp shuffles and then over the warps in warp order.  Deterministic.
+constexpr int kReduceThreads = 256;
+constexpr int kMaxUnitsPerReq = 1024;
+
+__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
+
+// CTA cta of ncta with NT threads; s_part holds NT / 32 * SPT floats and s_tile0 kMaxUnitsPerReq ints
+// of shared memory
+template <int SPT, bool HALVES, int NT>
+__device__ void reduce_tasks(const Params& P, int cta, int ncta, float* s_part, int* s_tile0) {
+    // sums per half-tile and per tile, reference maxima per tile (see halves_layout)
+    constexpr int NE = HALVES ? sub_blocks_per_half(kTileKeys / SPT) : SPT, SB = HALVES ? 2 * NE : SPT;
+    constexpr int NR = HALVES ? 2 : 1;
+    constexpr int B = SB <= 2 ? 4 : SB == 4 ? 2 : 1;         // (unit, row group) pairs per thread in flight
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const int upr = P.units_per_req, rows = P.slab_rows, rows4 = rows / 4;
+    const int pairs = upr * rows4;
+    const int req_items = __ldcg(P.n_items) / upr;          // items of unit 0 of every request
+    // each CTA takes a contiguous range of (request, key tile) tasks; the request changes rarely inside it
+    const int tasks = req_items * kItemTiles;
+    const int per = (tasks + ncta - 1) / ncta;
+    const int task0 = cta * per, task1 = min(tasks, task0 + per);
+    int r = -1, rbeg = 0, rend = 0, N = 0;
+    for (int task = task0; task < task1; ++task) {
+        if (task >= rend) {
+            // the request: the largest r whose first item (unit_items[r * upr].x / upr) is <= task / 2
+            const int ri = task / kItemTiles;
+            int lo = 0, hi = P.R;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (__ldcg(&P.unit_items[mid * upr].x) / upr <= ri) lo = mid; else hi = mid;
+            }
+            r = lo;
+            N = P.cu[r + 1] - P.cu[r];
+            const int2 u0 = __ldcg(&P.unit_items[r * upr]);
+            rbeg = (u0.x / upr) * kItemTiles;
+            rend = rbeg + u0.y * kItemTiles;
+            __syncthreads();                                    // the previous request's bases are no longer read
+            for (int kk = threadIdx.x; kk < upr; kk += NT)
+                s_tile0[kk] = __ldcg(&P.unit_items[r * upr + kk].x) * kItemTiles;
+            __syncthreads();
+        }
+        const int tile = task - rbeg;
+        if (N == 0 || tile * kTileKeys >= N) continue;     // the odd tile of a request's last item
+        float acc[SPT];
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
+        for (int i0 = threadIdx.x; i0 < pairs; i0 += B * NT) {
+            float4 wv[B][NR], ev[B][SB];
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+                const int i = i0 + b * NT;
+                bool live = i < pairs;
+                size_t t = 0;
+                int kk = 0, r0 = 0;
+                if (live) {
+                    kk = i / rows4;
+                    r0 = (i - kk * rows4) * 4;
+                    t = static_cast<size_t>(s_tile0[kk]) + tile;
+                    live = UP_IN((t * NR + NR - 1) * rows + r0 + 3, P.lim_bm, P.status) &&
+                           UP_IN((t * SB + SB - 1) * rows + r0 + 3, P.lim_be, P.status) &&
+                           UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status);
+                }
+                if (!live) {
+#pragma unroll
+                    for (int hh = 0; hh < NR; ++hh) wv[b][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int sb = 0; sb < SB; ++sb) ev[b][sb] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    continue;
+                }
+                const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
+#pragma unroll
+                for (int hh = 0; hh < NR; ++hh) {
+                    const float4 m4 = ldcg4(P.bm + (t * NR + hh) * rows + r0);
+                    wv[b][hh] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
+                }
+#pragma unroll
+                for (int sb = 0; sb < SB; ++sb) ev[b][sb] = ldcg4(P.be + (t * SB + sb) * rows + r0);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int sb = 0; sb < SB; ++sb) {
+                    const float4 w4 = wv[b][sb / NE], e4 = ev[b][sb];
+                    acc[SB == SPT ? sb : 0] += (e4.x * w4.x + e4.y * w4.y) + (e4.z * w4.z + e4.w * w4.w);
+                }
+        }
+#pragma unroll
+        for (int s = 0; s < SPT; ++s) {
+            float x = acc[s];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+            if (lane == 0) s_part[w * SPT + s] = x;
+        }
+        __syncthreads();
+        if (threadIdx.x < SPT) {
+            const int g = tile * SPT + threadIdx.x;
+            if (g * P.G < N) {
+                float x = 0.f;
+                for (int w2 = 0; w2 < NT / 32; ++w2) x += s_part[w2 * SPT + threadIdx.x];
+                const int ne = min(P.n, N);
+                if (UP_IN(P.cb[r] + g, P.nb_cap, P.status))
+                    P.block_scores[P.cb[r] + g] = x * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int SPT, bool HALVES>
+__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
+    pdl_wait();
+    pdl_trigger();
+    if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
+    __shared__ float s_part[kReduceThreads / 32 * SPT];
+    __shared__ int s_tile0[kMaxUnitsPerReq];
+    reduce_tasks<SPT, HALVES, kReduceThreads>(P, blockIdx.x, gridDim.x, s_part, s_tile0);
+}
+
+// PLAN (one pass only): the kernel plans its own items (plan_prologue) instead of reading the list of
+// the plan kernel.
+template <int PASS, int NC, bool PLAN = false>
 __global__ void __launch_bounds__(kThreads, 1)
     score_pass_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK, Params P) {
     extern __shared__ uint8_t smem_raw[];
@@ -1398,8 +1612,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
     }
-    // query rows that no TMA load ever writes (slab padding) must be finite: zero the slab once
-    for (int i = threadIdx.x; i < kSlabBytes / 16; i += kThreads) reinterpret_cast<uint4*>(S.slab)[i] = make_uint4(0, 0, 0, 0);
+    // query rows that no TMA load ever writes (slab padding) must be finite: zero the slab once (a
+    // planning pass uses its first kPlanScratch bytes as scratch and zeroes them after its prologue)
+    for (int i = (PLAN ? kPlanScratch / 16 : 0) + threadIdx.x; i < kSlabBytes / 16; i += kThreads)
+        reinterpret_cast<uint4*>(S.slab)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (warp == 1) {
         tmem_alloc(smem_u32(S.tmem_holder), kTmemCols);
@@ -1416,9 +1632,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // epilogue waits, for the row normalisers of its predecessor (the merge kernel).
     if (PASS != 2) pdl_wait();
     pdl_trigger();
-    const int n_items = uni(__ldcg(P.n_items));
     int it0, it1;
-    {
+    bool planned = true;
+    if (PLAN) {
+        int* scratch = reinterpret_cast<int*>(S.slab);
+        planned = plan_prologue(P, scratch, scratch + kPlanSmemReqs, it0, it1);
+        __syncthreads();                        // scratch no longer read; this CTA's item entries written
+        for (int i = threadIdx.x; i < kPlanScratch / 16; i += kThreads) reinterpret_cast<uint4*>(S.slab)[i] = make_uint4(0, 0, 0, 0);
+        fence_proxy_async_smem();
+        __syncthreads();
+    } else {
+        const int n_items = uni(__ldcg(P.n_items));
         // gridDim.x = nsets * groups: CTA (set s, group g) takes the g-th share of set s's run
         const int groups = gridDim.x / P.nsets, run = n_items / P.nsets;
         const int set = blockIdx.x / groups, g = blockIdx.x % groups;
@@ -1514,120 +1738,6 @@ __global__ void finalize_kernel(Params P) {
     }
 }
 
-// The one pass's Eq. 4: one CTA per (request, key tile) forms the tile's SPT = 128 / G block scores
-//   b_g = 1/(n_eff * Hq * G) * sum over the request's units and their rows j of e_{j,g} * 2^(m_t,j - c_j).
-// Threads take (unit, group of 4 rows) pairs in a fixed assignment, with 16-byte loads, several pairs'
-// loads in flight before any is used; per-thread sums are reduced by warp shuffles and then over the
-// warps in warp order.  Deterministic.
-constexpr int kReduceThreads = 256;
-constexpr int kMaxUnitsPerReq = 1024;
-
-__device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterpret_cast<const float4*>(p)); }
-
-template <int SPT, bool HALVES>
-__global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
-    pdl_wait();
-    pdl_trigger();
-    if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
-    // sums per half-tile and per tile, reference maxima per tile (see halves_layout)
-    constexpr int NE = HALVES ? sub_blocks_per_half(kTileKeys / SPT) : SPT, SB = HALVES ? 2 * NE : SPT;
-    constexpr int NR = HALVES ? 2 : 1;
-    constexpr int B = SB <= 2 ? 4 : SB == 4 ? 2 : 1;         // (unit, row group) pairs per thread in flight
-    __shared__ float s_part[kReduceThreads / 32][SPT];
-    __shared__ int s_tile0[kMaxUnitsPerReq];
-    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-    const int upr = P.units_per_req, rows = P.slab_rows, rows4 = rows / 4;
-    const int pairs = upr * rows4;
-    const int req_items = __ldcg(P.n_items) / upr;          // items of unit 0 of every request
-    // each CTA takes a contiguous range of (request, key tile) tasks; the request changes rarely inside it
-    const int tasks = req_items * kItemTiles;
-    const int per = (tasks + gridDim.x - 1) / gridDim.x;
-    const int task0 = blockIdx.x * per, task1 = min(tasks, task0 + per);
-    int r = -1, rbeg = 0, rend = 0, N = 0;
-    for (int task = task0; task < task1; ++task) {
-        if (task >= rend) {
-            // the request: the largest r whose first item (unit_items[r * upr].x / upr) is <= task / 2
-            const int ri = task / kItemTiles;
-            int lo = 0, hi = P.R;
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (P.unit_items[mid * upr].x / upr <= ri) lo = mid; else hi = mid;
-            }
-            r = lo;
-            N = P.cu[r + 1] - P.cu[r];
-            rbeg = (P.unit_items[r * upr].x / upr) * kItemTiles;
-            rend = rbeg + P.unit_items[r * upr].y * kItemTiles;
-            __syncthreads();                                    // the previous request's bases are no longer read
-            for (int kk = threadIdx.x; kk < upr; kk += kReduceThreads)
-                s_tile0[kk] = P.unit_items[r * upr + kk].x * kItemTiles;
-            __syncthreads();
-        }
-        const int tile = task - rbeg;
-        if (N == 0 || tile * kTileKeys >= N) continue;     // the odd tile of a request's last item
-        float acc[SPT];
-#pragma unroll
-        for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
-        for (int i0 = threadIdx.x; i0 < pairs; i0 += B * kReduceThreads) {
-            float4 wv[B][NR], ev[B][SB];
-#pragma unroll
-            for (int b = 0; b < B; ++b) {
-                const int i = i0 + b * kReduceThreads;
-                bool live = i < pairs;
-                size_t t = 0;
-                int kk = 0, r0 = 0;
-                if (live) {
-                    kk = i / rows4;
-                    r0 = (i - kk * rows4) * 4;
-                    t = static_cast<size_t>(s_tile0[kk]) + tile;
-                    live = UP_IN((t * NR + NR - 1) * rows + r0 + 3, P.lim_bm, P.status) &&
-                           UP_IN((t * SB + SB - 1) * rows + r0 + 3, P.lim_be, P.status) &&
-                           UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status);
-                }
-                if (!live) {
-#pragma unroll
-                    for (int hh = 0; hh < NR; ++hh) wv[b][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int sb = 0; sb < SB; ++sb) ev[b][sb] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    continue;
-                }
-                const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
-#pragma unroll
-                for (int hh = 0; hh < NR; ++hh) {
-                    const float4 m4 = ldcg4(P.bm + (t * NR + hh) * rows + r0);
-                    wv[b][hh] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
-                }
-#pragma unroll
-                for (int sb = 0; sb < SB; ++sb) ev[b][sb] = ldcg4(P.be + (t * SB + sb) * rows + r0);
-            }
-#pragma unroll
-            for (int b = 0; b < B; ++b)
-#pragma unroll
-                for (int sb = 0; sb < SB; ++sb) {
-                    const float4 w4 = wv[b][sb / NE], e4 = ev[b][sb];
-                    acc[SB == SPT ? sb : 0] += (e4.x * w4.x + e4.y * w4.y) + (e4.z * w4.z + e4.w * w4.w);
-                }
-        }
-#pragma unroll
-        for (int s = 0; s < SPT; ++s) {
-            float x = acc[s];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-            if (lane == 0) s_part[w][s] = x;
-        }
-        __syncthreads();
-        if (threadIdx.x < SPT) {
-            const int g = tile * SPT + threadIdx.x;
-            if (g * P.G < N) {
-                float x = 0.f;
-                for (int w2 = 0; w2 < kReduceThreads / 32; ++w2) x += s_part[w2][threadIdx.x];
-                const int ne = min(P.n, N);
-                if (UP_IN(P.cb[r] + g, P.nb_cap, P.status))
-                    P.block_scores[P.cb[r] + g] = x * (1.0f / (static_cast<float>(ne) * P.Hq * P.G));
-            }
-        }
-        __syncthreads();
-    }
-}
 
 // ------------------------------------------------------------------------------------------------
 // host
@@ -1696,11 +1806,25 @@ static cudaError_t launch_both(const CUtensorMap& q, const CUtensorMap& k, const
     return launch_pass<2, NC>(q, k, P, grid, st);
 }
 
-// one pass (row statistics and block sums), merge, reduce into the block scores
+// one pass (row statistics and block sums), merge, reduce into the block scores; plan_inside: the pass
+// plans its own items (no plan kernel before it)
 template <int NC>
 static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const Params& P, int grid,
-                              int64_t merge_rows, int64_t req_tiles, cudaStream_t st) {
-    cudaError_t e = launch_pass<3, NC>(q, k, P, grid, st);
+                              int64_t merge_rows, int64_t req_tiles, cudaStream_t st, bool plan_inside = false) {
+    cudaError_t e;
+    if (plan_inside) {
+        static std::once_flag once;
+        static cudaError_t attr = cudaSuccess;
+        std::call_once(once, [] {
+            attr = cudaFuncSetAttribute(score_pass_kernel<3, NC, true>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        });
+        if (attr != cudaSuccess) return attr;
+        e = launch_pdl(score_pass_kernel<3, NC, true>, dim3(grid), dim3(kThreads), kSmemBytes, st, q, k, P);
+        count_launch();
+    } else {
+        e = launch_pass<3, NC>(q, k, P, grid, st);
+    }
     if (e != cudaSuccess) return e;
     e = launch_merge(P, merge_rows, st);
     if (e != cudaSuccess) return e;
@@ -1798,6 +1922,22 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.status = dev_status;
     P.nsets = work_sets(P.units_per_req, g.slabs, num_sms());
 
+    // the one pass with at most kPlanSmemReqs requests plans inside its own launch
+    if (T > 0 && one_pass && R <= kPlanSmemReqs) {
+        CUtensorMap tq, tk;
+        if (!make_map(&tq, Q, T, Hq, dk, g.box_rows) || !make_map(&tk, K, T, Hkv, dk, kTileKeys)) return UP_ERR_CUDA;
+        int grid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(num_sms(), L.items_cap)));
+        grid = grid / P.nsets * P.nsets;
+        const int64_t merge_rows = L.units * g.slab_rows;
+        const int64_t req_tiles = L.items_cap / P.units_per_req * kItemTiles;
+        cudaError_t e;
+        switch (g.nc) {
+            case 1: e = launch_one<1>(tq, tk, P, grid, merge_rows, req_tiles, st, true); break;
+            case 2: e = launch_one<2>(tq, tk, P, grid, merge_rows, req_tiles, st, true); break;
+            default: e = launch_one<4>(tq, tk, P, grid, merge_rows, req_tiles, st, true); break;
+        }
+        return e == cudaSuccess ? UP_OK : UP_ERR_CUDA;
+    }
     // the item list by a grid of CTAs (one while the requests' offsets do not fit their shared memory)
     const int pgrid = R <= kPlanSmemReqs
                           ? static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(cdiv(L.items_cap, kPlanThreads), num_sms())))

@@ -261,6 +261,22 @@ def test_score_matches_oracle(case, tokens):
         parity.check_block_scores(step.token_scores.cpu().numpy(), s_ref)
 
 
+# up to 4,096 requests the one pass plans inside its single (fused) launch; beyond, a separate plan
+# kernel searches the request offsets in global memory
+@pytest.mark.parametrize("R", [4096, 4500])
+def test_score_with_many_requests_matches_oracle(R):
+    rng = np.random.default_rng(R)
+    lengths = tuple(int(x) for x in rng.integers(0, 48, R))
+    w = recipe.small(lengths=lengths, Hq=4, Hkv=2, dk=64, hdim=64, G=16, n=16, salt=R)
+    host = gen.materialize(w, with_hidden=False)
+    step, _ = _run_score(w, host, with_tokens=False)
+    Q = gen.bf16_bits_to_f32(host["Q"]).astype(np.float64)
+    K = gen.bf16_bits_to_f32(host["K"]).astype(np.float64)
+    s_ref = oracle.token_scores(Q, K, host["cu_seqlens"], w.n)
+    b_ref = oracle.block_scores_from_tokens(s_ref, host["cu_seqlens"], w.G)
+    parity.check_block_scores(step.block_scores.cpu().numpy()[:len(b_ref)], b_ref)
+
+
 @pytest.mark.parametrize("tokens", [True, False], ids=["two_pass", "one_pass"])
 def test_score_closed_form_at_q_zero(tokens):
     """Q = 0: the scores follow the closed form 1/(n_eff) sum 1/(j+1) whatever K is (block scores: the
