@@ -54,7 +54,7 @@ constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = idesc_bf16_f32(128, 128);
 constexpr uint32_t kIdescWide = idesc_bf16_f32(128, 256);
 constexpr int kCtrlBytes = 256;
-constexpr int kCvecFloats = 1024;
+constexpr int kCvecFloats = 2048;               // pass 2: row normalisers; one pass (d_k = 256): half exchange
 constexpr int kXchgBytes = 4 * 2 * 128 * 8;     // pass 1: (m,l) of 4 warpgroups x 2 jobs
 constexpr int kSmemBytes = 1024 + kSlabBytes + kStages * kStageBytes + kCtrlBytes + kCvecFloats * 4 + kXchgBytes;
 
@@ -82,8 +82,8 @@ struct Params {
     float* cvec;
     float* blk;
     float* tok;
-    float* be;             // one pass: per (unit, key tile, sub-block of the tile, row) sums of 2^(S*a - m_{t,h})
-    float* bm;             // one pass: per (unit, key tile, half-tile, row) the reference m_{t,h} of those sums
+    float* be;             // one pass: per (unit, key tile, block of the tile, row) block sums of 2^(S*a - m_t)
+    float* bm;             // one pass: per (unit, key tile, row) the reference m_t of those sums
     int spt;               // one pass: blocks per key tile (128 / G)
     // element counts of the workspace arrays (checked by the bounds-checked build)
     int64_t lim_items, lim_units, lim_ml, lim_cvec, lim_blk, lim_tok, lim_be, lim_bm;
@@ -118,14 +118,7 @@ __host__ __device__ __forceinline__ JobMap job_map(const Params& P) {
 __host__ __device__ constexpr bool one_pass_ok(int J) { return J == 1 || J == 2 || J == 4; }
 // Sub-block sums per half-tile (64 keys) of the one pass: the blocks of G <= 64 keys in it, or one.
 __host__ __device__ constexpr int sub_blocks_per_half(int G) { return G >= 64 ? 1 : 64 / G; }
-// The one pass's block sums and their reference maxima per (key tile, row): one maximum and 128 / G
-// sums ("whole" layout) for d_k <= 128, two maxima and the sub-block sums of both halves ("halves"
-// layout) for d_k = 256 (nc = d_k / 64 = 4); see the one-pass section below.
-__host__ __device__ constexpr bool halves_layout(int nc) { return nc == 4; }
-__host__ __device__ constexpr int refs_per_tile(int nc) { return halves_layout(nc) ? 2 : 1; }
-__host__ __device__ constexpr int sums_per_tile(int nc, int G) {
-    return halves_layout(nc) ? 2 * sub_blocks_per_half(G) : kTileKeys / G;
-}
+
 
 static bool geometry(int Hq, int Hkv, int dk, int n, Geometry* g) {
     if (Hq <= 0 || Hkv <= 0 || Hq % Hkv) return false;
@@ -170,8 +163,8 @@ static Layout layout(int R, int64_t T, const Geometry& g, int Hkv, int64_t nb_ca
         // block sums and their reference maxima of the one pass, per (unit, key tile, row); a unit's tiles
         // start at twice its first item's index in the plan's dense per-unit item numbering
         const size_t tiles = static_cast<size_t>(L.items_cap) * kItemTiles;
-        L.be = take(sizeof(float) * tiles * sums_per_tile(g.nc, G) * g.slab_rows);
-        L.bm = take(sizeof(float) * tiles * refs_per_tile(g.nc) * g.slab_rows);
+        L.be = take(sizeof(float) * tiles * (kTileKeys / G) * g.slab_rows);
+        L.bm = take(sizeof(float) * tiles * g.slab_rows);
     }
     L.total = o;
     return L;
@@ -1094,17 +1087,14 @@ __device__ void epilogue(const Params& P, const Smem& S, uint32_t tmem_base, int
 // ------------------------------------------------------------------------------------------------
 // the one pass: row statistics and block sums from a single Q.K^T
 //
-// Per window row j and key tile t, the thread that owns row j (rows are TMEM lanes) computes with its
-// running maximum m_t (base 2, over the keys it has seen up to the end of tile t) the sums
-//   e_{j,g} = sum_{i in B_g} 2^(S_ji * a - m_t)      for the 128 / G blocks g of tile t,
-// and writes them with m_t ("whole" layout, d_k <= 128).  At d_k = 256 each tile is read in two halves
-// of 64 keys by two threads that own row j ("halves" layout): the thread of half h keeps its own
-// running maximum m_{t,h} and writes the sums over the sub-blocks s of its half (the blocks of G <= 64
-// keys in it, or its 64 keys of a 128-key block) with m_{t,h}.  The (m, l) partials per work item
-// (merged over the threads that hold a row) are written as in pass 1, so the merge kernel gives
-// c_j = m_j + log2(l_j), and the reduce kernel then forms Eq. 4 exactly:
-//   sum_j sum_{i in B_g} A_ji = sum_j e_{j,g} * 2^(m_t - c_j)                   (whole)
-//                             = sum_j sum_{s in B_g} e_{j,s} * 2^(m_{t,h(s)} - c_j)   (halves).
+// Per window row j and key tile t, with a running maximum m_t (base 2, over the keys seen up to the end
+// of tile t) the epilogue computes the sums
+//   e_{j,g} = sum_{i in B_g} 2^(S_ji * a - m_t)      for the 128 / G blocks g of tile t
+// and writes them with m_t (at d_k = 256 the two threads that read the halves of row j's tile each sum
+// against their own maximum and rescale to the larger one before writing).  The (m, l) partials per
+// work item (merged over the threads that hold a row) are written as in pass 1, so the merge kernel
+// gives c_j = m_j + log2(l_j), and the reduce kernel then forms Eq. 4 exactly:
+//   sum_j sum_{i in B_g} A_ji = sum_j e_{j,g} * 2^(m_t - c_j).
 // This is the two-pass softmax of the section 3.5 kernel design with the second pass run over the block
 // sums (G times smaller than S) instead of over a recomputed S: the tensor work and the exponentials of
 // the recompute pass disappear; S itself is never stored.
@@ -1302,109 +1292,116 @@ __device__ void epilogue_one_pass_whole(const Params& P, const Smem& S, uint32_t
     }
 }
 
-// d_k = 256 (the chunks-outer issue order): the four epilogue warpgroups form two pairs; pair p drains
-// the jobs q (running job count) with
-// q mod 2 = p, which are those in TMEM buffers p and p + 2, and in each job warpgroup 2p + h reads
-// the columns 64h .. 64h + 63.  With J = 4 jobs per tile a pair holds the rows of jobs p and p + 2 (two
-// rows per thread), with J = 2 those of job p, and with J = 1 the pairs take alternate tiles of the
-// one job.  A job is drained by eight warps, so its TMEM buffer comes free in about half the time one
-// warpgroup takes, and consecutive jobs (issued in order, see mma_issuer) drain on different pairs:
-// the exponentials of one job overlap the MMAs of the next.  The threads that hold a row merge their
-// (m, l) at the end of each item in a fixed order, as in pass 1.  CPB = G / 16.
+// d_k = 256 (the chunks-outer issue order, J = 1 or 2 jobs per tile): the four epilogue warpgroups
+// form two pairs; pair p drains the jobs q (running job count) with q mod 2 = p, which are those in
+// TMEM buffers p and p + 2, and in each job warpgroup 2p + h reads the columns 64h .. 64h + 63.  With
+// J = 2 a pair holds the rows of job p; with J = 1 the pairs take alternate tiles of the one job.  A
+// job is drained by eight warps, so its TMEM buffer comes free in about half the time one warpgroup
+// takes, and consecutive jobs drain on different pairs.  Each half keeps its own running maximum; at
+// the end of a job the two threads of a row trade (maximum, sum) through shared memory and write the
+// tile's block sums against the larger maximum, so the output is the same (m_t, e_{j,g}) as with one
+// thread per row.  The threads that hold a row merge their (m, l) at the end of each item in a fixed
+// order, as in pass 1.  CPB = G / 16.
 template <int CPB>
 __device__ void epilogue_one_pass_pairs(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1) {
-    constexpr int NE = sub_blocks_per_half(16 * CPB);   // sub-block sums per half-tile
-    constexpr int SB = 2 * NE;                          // per tile
+    constexpr int NE = sub_blocks_per_half(16 * CPB);   // sums per half-tile: its blocks, or half of one
+    constexpr int SPT = 8 / CPB;                         // blocks per tile
     volatile int* abort_flag = S.abort_flag;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wg = (warp - 2) >> 2;             // warpgroup 0..3
     const int pair = wg >> 1, h = wg & 1;       // jobs q with q % 2 == pair; columns 64h ..
     const int qd = warp & 3;                    // TMEM lane quarter this warp may access
     const int rl = qd * 32 + lane;
-    const int J = P.J;
-    const int nrow = J >= 2 ? J / 2 : 1;        // rows (jobs) per thread
+    const int J = P.J;                          // 1 or 2
+    const int job = J == 2 ? pair : 0;          // the job (128 rows of the slab) of this thread's row
+    const int row = job * 128 + rl;
     const float a = P.a;
     const uint32_t ta0 = tmem_base + (static_cast<uint32_t>(qd * 32) << 16) + 64 * h;
-    auto job_of = [&](int u) { return J >= 2 ? pair + 2 * u : 0; };
-    uint32_t tiles_done = 0;
+    uint32_t tiles_done = 0, jn = 0;
     int prev_slab = -1;
-    bool rin[2] = {false, false};
-    int rmod[2] = {0, 0};
+    bool rin = false;
+    int rmod = 0;
     for (int it = it0; it < it1; ++it) {
         int4 ia, ib;
         item_load(P, it, it1, ia, ib);
         const ItemInfo I = item_decode(P, ia, ib);
         if (I.slab != prev_slab) {
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (u >= nrow) break;
-                const int qg = I.slab * P.slab_rows + job_of(u) * 128 + rl;
-                rin[u] = qg < P.rows_total;
-                rmod[u] = qg % P.n;
-            }
+            const int qg = I.slab * P.slab_rows + row;
+            rin = qg < P.rows_total;
+            rmod = qg % P.n;
             prev_slab = I.slab;
         }
+        const int pos = I.N - P.n + rmod;       // this row's position in the request
+        const bool rvalid = rin && pos >= 0;
         const int2 ui = I.ui;
         const size_t tile0 = static_cast<size_t>(ui.x) * kItemTiles;   // the unit's first key tile
-        float m[2] = {-INFINITY, -INFINITY}, l[2] = {0.f, 0.f};
+        float m = -INFINITY, l = 0.f;
         for (int kt = I.tb; kt < I.te; ++kt, ++tiles_done) {
+            const uint32_t q = tiles_done * J + job;
+            if ((q & 1u) != static_cast<uint32_t>(pair)) continue;          // the other pair's tile (J = 1)
+            const uint32_t buf = q & 3u;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (q >> 2) & 1, abort_flag));
+            tc_fence_after();
+            float e[NE];
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                if (u >= nrow) break;
-                const uint32_t q = tiles_done * J + job_of(u);
-                if ((q & 1u) != static_cast<uint32_t>(pair)) continue;          // the other pair's tile (J = 1)
-                const uint32_t buf = q & 3u;
-                const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(S.tfull + buf), (q >> 2) & 1, abort_flag));
-                tc_fence_after();
-                if (!ok) {
-                    release_tmem(S, buf, lane);
-                    continue;
-                }
-                const int row = job_of(u) * 128 + rl;
-                const int pos = I.N - P.n + rmod[u];                         // this row's position in the request
-                const int lim = rin[u] && pos >= 0 ? pos - kt * kTileKeys - 64 * h : -1;   // last visible column
-                float e[NE];
-#pragma unroll
-                for (int b = 0; b < NE; ++b) e[b] = 0.f;
+            for (int b = 0; b < NE; ++b) e[b] = 0.f;
+            if (ok) {
+                const int lim = rvalid ? pos - kt * kTileKeys - 64 * h : -1;      // last visible column
                 const bool masked = !__all_sync(0xffffffffu, lim >= 63);
-                one_pass_half<CPB, NE>(S, ta0 + buf * 128, buf, lane, masked, lim, a, m[u], l[u], e);
-                const size_t t = tile0 + kt;
-                const size_t mi = (t * 2 + h) * P.slab_rows + row;
-                if (UP_IN(mi, P.lim_bm, P.status)) P.bm[mi] = m[u];
-                float ts = 0.f;
+                one_pass_half<CPB, NE>(S, ta0 + buf * 128, buf, lane, masked, lim, a, m, l, e);
+            } else {
+                release_tmem(S, buf, lane);
+            }
+            // the other half's (maximum, sum): double-buffered by job so that one pair barrier per job
+            // suffices (a half writes job k + 2's entry only after both passed job k + 1's barrier);
+            // every thread of the pair reaches it, whatever `ok` was
+            float2* xj = reinterpret_cast<float2*>(S.cvec) + ((jn & 1u) * 2 + pair) * 256;   // [half][128]
+            xj[h * 128 + rl] = make_float2(m, e[0]);
+            named_bar_sync(1 + pair, kEpiThreads / 2);
+            const float2 o = xj[(h ^ 1) * 128 + rl];
+            ++jn;
+            const float M = fmaxf(m, o.x);
+            const float sc = m == -INFINITY ? 0.f : ex2(m - M);               // this half's sums to M
+            const size_t t = tile0 + kt;
+            float ts = 0.f;
+#pragma unroll
+            for (int b = 0; b < NE; ++b) ts += e[b];
+            l += ts;
+            if (!ok) continue;
+            if (SPT == 1) {
+                // G = 128: the tile's one block spans both halves
+                if (h == 0) {
+                    const float so = o.x == -INFINITY ? 0.f : ex2(o.x - M);
+                    if (UP_IN(t * P.slab_rows + row, P.lim_be, P.status)) P.be[t * P.slab_rows + row] = e[0] * sc + o.y * so;
+                }
+            } else {
 #pragma unroll
                 for (int b = 0; b < NE; ++b) {
-                    const size_t ei = (t * SB + h * NE + b) * P.slab_rows + row;
-                    if (UP_IN(ei, P.lim_be, P.status)) P.be[ei] = e[b];
-                    ts += e[b];
+                    const size_t ei = (t * SPT + h * NE + b) * P.slab_rows + row;
+                    if (UP_IN(ei, P.lim_be, P.status)) P.be[ei] = e[b] * sc;
                 }
-                l[u] += ts;
             }
+            if (h == 0 && UP_IN(t * P.slab_rows + row, P.lim_bm, P.status)) P.bm[t * P.slab_rows + row] = M;
         }
-        // this item's (m, l) partial of each row, merged over the threads that hold the row: the two
-        // halves of its pair (a barrier of the pair only, so that the pairs stay independent), and with
-        // J = 1 both pairs
+        // this item's (m, l) partial of the row, merged over the threads that hold it: the two halves of
+        // its pair (a barrier of the pair only, so that the pairs stay independent), and with J = 1 both
+        // pairs
         float2* part = P.ml + (size_t)ui.x * P.slab_rows + I.tb / kItemTiles;
-        float2* xm = reinterpret_cast<float2*>(S.xchg);                      // [4 warpgroups][2 rows][128]
-#pragma unroll
-        for (int u = 0; u < 2; ++u)
-            if (u < nrow) xm[(wg * 2 + u) * 128 + rl] = make_float2(m[u], l[u]);
-        const int bar_id = J >= 2 ? 1 + pair : 3, bar_n = J >= 2 ? kEpiThreads / 2 : kEpiThreads;
+        float2* xm = reinterpret_cast<float2*>(S.xchg);                      // [4 warpgroups][128]
+        xm[wg * 128 + rl] = make_float2(m, l);
+        const int bar_id = J == 2 ? 1 + pair : 3, bar_n = J == 2 ? kEpiThreads / 2 : kEpiThreads;
         named_bar_sync(bar_id, bar_n);
-        const int wfirst = J >= 2 ? 2 * pair : 0, wcount = J >= 2 ? 2 : 4;
+        const int wfirst = J == 2 ? 2 * pair : 0, wcount = J == 2 ? 2 : 4;
         if (wg == wfirst) {
-            for (int u = 0; u < nrow; ++u) {        // (m, l) from shared memory: no register arrays indexed here
-                float mm = -INFINITY;
-                for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) mm = fmaxf(mm, xm[(w2 * 2 + u) * 128 + rl].x);
-                float ll = 0.f;
-                if (mm > -INFINITY)
-                    for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) {
-                        const float2 x = xm[(w2 * 2 + u) * 128 + rl];
-                        ll += x.y * ex2(x.x - mm);
-                    }
-                const int row = job_of(u) * 128 + rl;
-                if (UP_IN(part + (size_t)row * ui.y - P.ml, P.lim_ml, P.status)) part[(size_t)row * ui.y] = make_float2(mm, ll);
-            }
+            float mm = -INFINITY;
+            for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) mm = fmaxf(mm, xm[w2 * 128 + rl].x);
+            float ll = 0.f;
+            if (mm > -INFINITY)
+                for (int w2 = wfirst; w2 < wfirst + wcount; ++w2) {
+                    const float2 x = xm[w2 * 128 + rl];
+                    ll += x.y * ex2(x.x - mm);
+                }
+            if (UP_IN(part + (size_t)row * ui.y - P.ml, P.lim_ml, P.status)) part[(size_t)row * ui.y] = make_float2(mm, ll);
         }
         named_bar_sync(bar_id, bar_n);
     }
@@ -1471,12 +1468,9 @@ __device__ __forceinline__ float4 ldcg4(const float* p) { return __ldcg(reinterp
 
 // CTA cta of ncta with NT threads; s_part holds NT / 32 * SPT floats and s_tile0 kMaxUnitsPerReq ints
 // of shared memory
-template <int SPT, bool HALVES, int NT>
+template <int SPT, int NT>
 __device__ void reduce_tasks(const Params& P, int cta, int ncta, float* s_part, int* s_tile0) {
-    // sums per half-tile and per tile, reference maxima per tile (see halves_layout)
-    constexpr int NE = HALVES ? sub_blocks_per_half(kTileKeys / SPT) : SPT, SB = HALVES ? 2 * NE : SPT;
-    constexpr int NR = HALVES ? 2 : 1;
-    constexpr int B = SB <= 2 ? 4 : SB == 4 ? 2 : 1;         // (unit, row group) pairs per thread in flight
+    constexpr int B = SPT <= 2 ? 4 : SPT == 4 ? 2 : 1;       // (unit, row group) pairs per thread in flight
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
     const int upr = P.units_per_req, rows = P.slab_rows, rows4 = rows / 4;
     const int pairs = upr * rows4;
@@ -1511,7 +1505,7 @@ __device__ void reduce_tasks(const Params& P, int cta, int ncta, float* s_part, 
 #pragma unroll
         for (int s = 0; s < SPT; ++s) acc[s] = 0.f;
         for (int i0 = threadIdx.x; i0 < pairs; i0 += B * NT) {
-            float4 wv[B][NR], ev[B][SB];
+            float4 wv[B], ev[B][SPT];
 #pragma unroll
             for (int b = 0; b < B; ++b) {
                 const int i = i0 + b * NT;
@@ -1522,32 +1516,28 @@ __device__ void reduce_tasks(const Params& P, int cta, int ncta, float* s_part, 
                     kk = i / rows4;
                     r0 = (i - kk * rows4) * 4;
                     t = static_cast<size_t>(s_tile0[kk]) + tile;
-                    live = UP_IN((t * NR + NR - 1) * rows + r0 + 3, P.lim_bm, P.status) &&
-                           UP_IN((t * SB + SB - 1) * rows + r0 + 3, P.lim_be, P.status) &&
+                    live = UP_IN(t * rows + r0 + 3, P.lim_bm, P.status) &&
+                           UP_IN((t * SPT + SPT - 1) * rows + r0 + 3, P.lim_be, P.status) &&
                            UP_IN(static_cast<size_t>(r * upr + kk) * rows + r0 + 3, P.lim_cvec, P.status);
                 }
                 if (!live) {
+                    wv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                    for (int hh = 0; hh < NR; ++hh) wv[b][hh] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int sb = 0; sb < SB; ++sb) ev[b][sb] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int sb = 0; sb < SPT; ++sb) ev[b][sb] = make_float4(0.f, 0.f, 0.f, 0.f);
                     continue;
                 }
                 const float4 c4 = ldcg4(P.cvec + static_cast<size_t>(r * upr + kk) * rows + r0);
+                const float4 m4 = ldcg4(P.bm + t * rows + r0);
+                wv[b] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
 #pragma unroll
-                for (int hh = 0; hh < NR; ++hh) {
-                    const float4 m4 = ldcg4(P.bm + (t * NR + hh) * rows + r0);
-                    wv[b][hh] = make_float4(ex2(m4.x - c4.x), ex2(m4.y - c4.y), ex2(m4.z - c4.z), ex2(m4.w - c4.w));
-                }
-#pragma unroll
-                for (int sb = 0; sb < SB; ++sb) ev[b][sb] = ldcg4(P.be + (t * SB + sb) * rows + r0);
+                for (int sb = 0; sb < SPT; ++sb) ev[b][sb] = ldcg4(P.be + (t * SPT + sb) * rows + r0);
             }
 #pragma unroll
             for (int b = 0; b < B; ++b)
 #pragma unroll
-                for (int sb = 0; sb < SB; ++sb) {
-                    const float4 w4 = wv[b][sb / NE], e4 = ev[b][sb];
-                    acc[SB == SPT ? sb : 0] += (e4.x * w4.x + e4.y * w4.y) + (e4.z * w4.z + e4.w * w4.w);
+                for (int sb = 0; sb < SPT; ++sb) {
+                    const float4 w4 = wv[b], e4 = ev[b][sb];
+                    acc[sb] += (e4.x * w4.x + e4.y * w4.y) + (e4.z * w4.z + e4.w * w4.w);
                 }
         }
 #pragma unroll
@@ -1572,14 +1562,14 @@ __device__ void reduce_tasks(const Params& P, int cta, int ncta, float* s_part, 
     }
 }
 
-template <int SPT, bool HALVES>
+template <int SPT>
 __global__ void __launch_bounds__(kReduceThreads) reduce_kernel(Params P) {
     pdl_wait();
     pdl_trigger();
     if (__ldcg(P.n_items + 1) == 0) return;   // plan rejected the varlen metadata
     __shared__ float s_part[kReduceThreads / 32 * SPT];
     __shared__ int s_tile0[kMaxUnitsPerReq];
-    reduce_tasks<SPT, HALVES, kReduceThreads>(P, blockIdx.x, gridDim.x, s_part, s_tile0);
+    reduce_tasks<SPT, kReduceThreads>(P, blockIdx.x, gridDim.x, s_part, s_tile0);
 }
 
 // PLAN (one pass only): the kernel plans its own items (plan_prologue) instead of reading the list of
@@ -1829,12 +1819,11 @@ static cudaError_t launch_one(const CUtensorMap& q, const CUtensorMap& k, const 
     e = launch_merge(P, merge_rows, st);
     if (e != cudaSuccess) return e;
     const int rgrid = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(req_tiles, 8 * num_sms())));
-    constexpr bool H = halves_layout(NC);
     switch (P.spt) {
-        case 8: e = launch_pdl(reduce_kernel<8, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        case 4: e = launch_pdl(reduce_kernel<4, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        case 2: e = launch_pdl(reduce_kernel<2, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
-        default: e = launch_pdl(reduce_kernel<1, H>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 8: e = launch_pdl(reduce_kernel<8>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 4: e = launch_pdl(reduce_kernel<4>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        case 2: e = launch_pdl(reduce_kernel<2>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
+        default: e = launch_pdl(reduce_kernel<1>, dim3(rgrid), dim3(kReduceThreads), 0, st, P); break;
     }
     count_launch();
     return e;
@@ -1915,8 +1904,8 @@ extern "C" up_status up_score_blocks(const uint16_t* Q, const uint16_t* K, const
     P.lim_cvec = L.units * g.slab_rows;
     P.lim_blk = static_cast<int64_t>(Hkv) * g.slabs * 4 * nb_cap;
     P.lim_tok = token_scores ? static_cast<int64_t>(Hkv) * g.slabs * 4 * T : 0;
-    P.lim_be = one_pass ? L.items_cap * kItemTiles * sums_per_tile(g.nc, G) * g.slab_rows : 0;
-    P.lim_bm = one_pass ? L.items_cap * kItemTiles * refs_per_tile(g.nc) * g.slab_rows : 0;
+    P.lim_be = one_pass ? L.items_cap * kItemTiles * (kTileKeys / G) * g.slab_rows : 0;
+    P.lim_bm = one_pass ? L.items_cap * kItemTiles * g.slab_rows : 0;
     P.block_scores = block_scores;
     P.token_scores = token_scores;
     P.status = dev_status;
