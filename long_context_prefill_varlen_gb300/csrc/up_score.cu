@@ -1206,7 +1206,7 @@ __device__ __forceinline__ void one_pass_tile(const Smem& S, uint32_t ta, uint32
 
 // d_k <= 128 (the jobs-outer issue order): warpgroup w drains TMEM buffer w whole; with J in {1, 2, 4}
 // jobs per tile that is always job w % J (the same 128 window rows), on every (4 / J)-th tile of the
-// CTA's sequence.  (The pairs of epilogue_one_pass_pairs measured 17-30% slower here: a thread then
+// CTA's sequence.  (The pairs of epilogue_one_pass_pairs measured 20-35% slower here: a thread then
 // pays the first TMEM load and the per-job bookkeeping twice per tile.)  The warpgroups that hold the
 // same rows merge their (m, l) at the end of each item in a fixed order, as in pass 1.  CPB = G / 16.
 template <int CPB>
