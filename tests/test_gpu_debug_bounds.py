@@ -19,7 +19,7 @@ from synth import recipe
 
 pytestmark = pytest.mark.gpu
 
-# Hq, Hkv, dk, G, n, lengths: jobs of 1, 2, 4 and 8 per tile, every G, and streams of at most 8, at
+# Hq, Hkv, dk, G, n, lengths: jobs of 1, 2, 4 and 8 per tile (and 1 at d_k = 256), every G, and streams of at most 8, at
 # most 64 and more than 64 tiles of 1,024 tokens for the compaction's three launch paths
 CASES = [
     (8, 2, 128, 64, 128, (700, 1500, 90, 333)),
@@ -29,6 +29,7 @@ CASES = [
     (4, 2, 256, 128, 256, (900, 300)),
     (2, 1, 64, 64, 128, (9000, 1, 2500)),
     (2, 1, 64, 64, 128, (70000, 500)),
+    (4, 4, 256, 16, 64, (1200, 70)),
 ]
 
 

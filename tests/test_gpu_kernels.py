@@ -228,6 +228,10 @@ SCORE_CASES = [
     # divide the SMs, so the 2 slabs of a head form the CTA sets; 16 one-slab units, the plain order
     (32, 8, 128, 64, 256, (1300, 600)),
     (16, 16, 128, 64, 128, (900, 70, 1500)),
+    # d_k = 256 with one job per key tile (the two epilogue pairs take alternate tiles), G = 16 (four
+    # blocks per half-tile) and n = 64
+    (8, 8, 256, 16, 128, (1500, 300)),
+    (4, 2, 256, 64, 64, (700, 90, 1)),
 ]
 
 
