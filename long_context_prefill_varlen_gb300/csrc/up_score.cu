@@ -397,6 +397,10 @@ struct Smem {
     uint8_t* xchg;         // [kXchgBytes]
 };
 
+// the barriers (full, empty, tfull, tempty, slab_full, slab_free, mma_done, tok), the TMEM address and the
+// abort flag fit the control block
+static_assert((2 * kStages + 8 + 2 + kIssuers + 2) * 8 + 8 <= kCtrlBytes, "control block too small");
+
 __device__ __forceinline__ Smem carve(uint8_t* raw) {
     Smem s;
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
