@@ -107,8 +107,10 @@ up_status up_make_cu_blocks(const int32_t* cu_seqlens, int R, int64_t T, int G,
  *     b_g  = 1/G * sum_{i in B_g} s_i     (B_g = {gG .. min((g+1)G, N)-1}; the last block is
  *                                          still divided by G)         [UP Eq. 4]
  *   kv(h) = h / (Hq / Hkv).  The softmax normalises over the complete key range before any
- *   block reduction, via two passes (row max/sum, then recompute) [UP 3.5 "Kernel design"];
- *   S is never materialised.
+ *   block reduction, in two passes [UP 3.5 "Kernel design"]: one pass over S gives each row's
+ *   maximum and sum and its sums over every block against a running maximum, and the second pass
+ *   runs over those block sums with the row normalisers (with token_scores, the second pass
+ *   recomputes S instead).  S is never materialised.
  * Q: bf16 [T, Hq, dk] (only each request's last n rows are read); K: bf16 [T, Hkv, dk]; both may
  * be NULL when T = 0.
  * Both 16-byte aligned.  dk in {64, 128, 256}; Hq % Hkv == 0; G in {16, 32, 64, 128};
