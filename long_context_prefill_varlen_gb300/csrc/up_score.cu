@@ -15,10 +15,10 @@
 //           per-(unit, block) partials; the final kernel divides by n_eff * Hq * G.
 // a = sm_scale * log2(e): the softmax is computed in base 2, exactly equal to exp in base e.
 //
-// CTA layout (640 threads, one CTA per SM, persistent over a contiguous range of work items):
+// CTA layout (608 threads, one CTA per SM, persistent over a contiguous range of work items):
 //   warp 0     TMA producer: the query slab of the current unit, then K tiles into a 5-stage ring
-//   warps 1, 18, 19  tcgen05.mma issuers (warp 1 also allocates TMEM; each runs its loop on the whole
-//              warp and issues from one elected lane), see mma_issuer
+//   warps 1, 18  tcgen05.mma issuers (warp 1 also allocates TMEM; each runs its loop on the whole warp
+//              and issues from one elected lane), see mma_issuer
 //   warps 2-17 four epilogue warpgroups.  A job is one 128 x W fp32 accumulator (W = 128 query rows;
 //              W = 256 in pass 2 when the slab has 256 rows).  One pass: warpgroup w drains TMEM
 //              buffer w whole at d_k <= 128, and at d_k = 256 the pairs of warpgroups drain alternate
@@ -45,7 +45,7 @@ constexpr int kStages = 5;
 constexpr int kSlabBytes = 128 * 1024;          // resident query rows of one unit
 constexpr int kItemTiles = 2;                   // key tiles per work item (pass-1 partial granularity)
 constexpr int kEpiThreads = 512;
-constexpr int kIssuers = 3;                     // MMA issuer warps (warps 1, 18 and 19); see mma_issuer
+constexpr int kIssuers = 2;                     // MMA issuer warps (warps 1 and 18); see mma_issuer
 constexpr int kEpiWarp0 = 2;                    // epilogue warps 2..17
 constexpr int kIssuer1Warp = kEpiWarp0 + kEpiThreads / 32;
 constexpr int kThreads = 64 + kEpiThreads + 32 * (kIssuers - 1);
@@ -536,23 +536,26 @@ __device__ void producer(const Params& P, const Smem& S, const CUtensorMap* tmQ,
 // the advance is a plain add on the descriptor.
 __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
-// Three issuer warps.  A tcgen05.mma returns to its thread only once the tensor core's queue has room
+// Two issuer warps.  A tcgen05.mma returns to its thread only once the tensor core's queue has room
 // (about five 128 x 128 x 16 steps, ~320 cycles of work), so an issuer runs at most that far ahead of
 // the pipe; a commit returns after ~55 cycles but holds the thread's next MMAs until the ones it tracks
 // have completed (timed on this part: ~80 idle cycles per commit when no other thread's MMAs are
-// queued).  Several issuers keep the queue filled across each other's commits and waits.
-//   jobs outer (d_k <= 128)  issuers 0 and 1 take the even and odd jobs of the running job count (TMEM
-//       buffers 0, 2 and 1, 3) and hand the turn to issue to each other through an mbarrier after
+// queued).  Two issuers keep the queue filled across each other's commits and waits.  Issuer w
+// issues the jobs q (running job count) with q mod 2 = w, i.e. those in TMEM buffers w and w + 2
+// (w alone for the two 256-column buffers of a wide pass).
+//   jobs outer (d_k <= 128)  the two also hand each other the turn to issue through an mbarrier after
 //       each job, so the tensor core receives whole jobs in order and they complete one after
 //       another, while each issuer's commit, buffer wait and loop overlap the other's MMAs.
-//   chunks outer (d_k = 256)  issuer w issues the jobs whose buffer b has b mod 3 == w.
+//   chunks outer (d_k = 256)  with J = 2 each issuer has one job per key tile; per K stage both issue
+//       their job's MMAs.  (A third issuer warp, the buffers handed out by b mod 3, measured 5-6% slower
+//       with this epilogue; with one issuer per buffer a 21st warp would cut the registers to 80.)
 // Every use of a TMEM buffer comes from the same warp in order, so its waits for the buffer always
 // refer to the phase just before the current one.  A commit tracks only its own thread's MMAs, so
 // every barrier that releases an operand (K stage, query slab) takes one commit from each issuer,
 // and each issuer waits for a stage to land before it commits the stage's release, even when it
 // issued no job on that tile: its arrival can then never count toward a later use of the stage.
-static_assert(kThreads == 640 && kIssuer1Warp + kIssuers - 2 == kThreads / 32 - 1,
-              "warps: producer 0, issuers 1, 18 and 19, epilogue 2-17");
+static_assert(kThreads == 608 && kIssuer1Warp + kIssuers - 2 == kThreads / 32 - 1,
+              "warps: producer 0, issuers 1 and 18, epilogue 2-17");
 template <int PASS, int NC>
 __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, int it0, int it1, uint32_t w) {
     volatile int* abort_flag = S.abort_flag;
@@ -575,9 +578,8 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
         if (leader) tc_commit(bar);
         __syncwarp();
     };
-    // chunks outer: buffer b by issuer b mod kIssuers (with jobs handed out round-robin an issuer could
-    // run two uses ahead on a buffer and read its parity from the wrong phase)
-    auto mine = [&](uint32_t q) { return (q & (jm.nbuf - 1)) % kIssuers == w; };
+    // job q by issuer q mod 2: its buffer is b = q mod nbuf, so buffer b always by issuer b mod 2
+    auto mine = [&](uint32_t q) { return (q & 1u) == w; };
     int4 na, nb;
     item_load(P, it0, it1, na, nb);
     for (int it = it0; it < it1; ++it) {
@@ -596,7 +598,7 @@ __device__ void mma_issuer(const Params& P, const Smem& S, uint32_t tmem_base, i
                 bool landed = false;
                 for (int j = 0; j < J; ++j) {
                     const uint32_t q = jc + j, buf = q & (jm.nbuf - 1);
-                    if ((q & 1u) != w) continue;
+                    if (!mine(q)) continue;
                     if (!wait_all(smem_u32(S.tempty + buf), ((q >> jm.nb_log) & 1) ^ 1)) goto out;
                     // this issuer's turn: the other one has issued job q - 1 (issuer 0's first job has no wait)
                     const int turn = static_cast<int>(q >> 1) - (w == 0 ? 1 : 0);
@@ -1647,7 +1649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         producer<NC>(P, S, &tmQ, &tmK, it0, it1);
     } else if (warp == 1 || warp >= kIssuer1Warp) {
-        // warps 1, 18 and 19 (kThreads covers exactly these and the producer and epilogue warps)
+        // warps 1 and 18 (kThreads covers exactly these and the producer and epilogue warps)
         mma_issuer<PASS, NC>(P, S, tmem_base, it0, it1, warp == 1 ? 0u : static_cast<uint32_t>(warp - kIssuer1Warp + 1));
     } else if (PASS == 3 && NC == 4) {
         switch (P.spt) {                         // blocks per key tile = 128 / G
